@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE dispatch / combine hot path on GB300.
+
+One step = ep_get_layout + ep_dispatch + ep_combine over one batch of
+synthetic tokens (workloads.py).  Default workload: "decode" (T=128, H=7168,
+E=256 as 32 partitions x 8, top-8, fp8 e4m3 dispatch into a [256,128,7168]
+capacity buffer, bf16 combine).
+
+Metric: effective HBM GB/s of the step = algorithmic bytes (what the method
+must move; see algorithmic_bytes) / device time, plus per-kernel us/call, GB/s
+and fraction of the measured HBM copy bandwidth.
+
+Timing: inputs resident in HBM; the L2 (129 MB) is flushed by writing a
+512 MB buffer before every timed step; each step is one CUDA-graph replay of
+the three calls, bracketed by CUDA events on the launching stream.  Kernels
+are also timed one at a time the same way.  e2e: the same step through the
+public API with pinned host inputs, host->device copies and the device->host
+read of the combined output inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference   # the CPU oracle on the same workload
+
+Multi-GPU: replicas (the single-GPU path has no exchange step); every rank
+runs the full workload on its own GPU, value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "dispatch/combine µs/call and effective HBM GB/s (1 GB300), % of HBM peak"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(wl: W.Workload, n_live: int) -> dict:
+    """Bytes each kernel must move, counted once (no padding, no re-reads).
+
+    layout:   read topk_idx, write slot_of, src_token/src_k for every receive
+              row, counts/offsets/partition arrays.
+    dispatch: read x once; write every live copy (bf16: H*2 bytes; fp8: H
+              bytes + H/128 f32 scales).
+    combine:  read every live row of y and topk_w / slot_of; write out.
+    """
+    T, H, k, E, P = wl.T, wl.H, wl.k, wl.E, wl.P
+    N = T * k
+    layout = 4 * N + 4 * N + 8 * wl.R + 4 * (2 * E + 2 * P + 2)
+    if wl.fp8:
+        dispatch = T * H * 2 + n_live * H + n_live * (H // 128) * 4
+    else:
+        dispatch = T * H * 2 + n_live * H * 2
+    combine = n_live * H * 2 + T * H * 2 + T * k * (4 + 4)
+    return dict(layout=layout, dispatch=dispatch, combine=combine)
+
+
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_ep_get_04_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (profiles/traffic.txt)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_source_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split("#", 1)[0].split()
+            if len(parts) == 4 and parts[0] == workload and parts[1] == kernel and parts[3] == digest:
+                return float(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the benchmark runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), sm_max=float(parts[1]), power=float(parts[2]),
+                                 hw=parts[4], hw_thermal=parts[5], sw_thermal=parts[6], sw_power=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 0.25 * max(r2["power"] for r2 in rows)] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in busy), sm_max_mhz=max(r["sm_max"] for r in busy),
+                    samples=len(busy), reasons=sorted(reasons))
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_step(wl: W.Workload, inp: dict, y: np.ndarray):
+    import oracle
+    mode = oracle.CAPACITY if wl.mode == W.CAPACITY else oracle.PACKED
+    L = oracle.layout(inp["topk_idx"], wl.E, wl.P, mode, wl.capacity)
+    if wl.fp8:
+        oracle.dispatch_fp8(inp["x"], L["slot_of"], wl.R)
+    else:
+        oracle.dispatch_bf16(inp["x"], L["slot_of"], wl.R)
+    oracle.combine(y, inp["topk_w"], L["slot_of"])
+
+
+def oracle_sample(wl: W.Workload, step_seconds: float = 1.0):
+    """A bounded sample of the workload for the oracle: its first T' tokens,
+    T' chosen so that one oracle step takes about step_seconds."""
+    probe = wl.shrink(min(wl.T, 16))
+    inp = W.make(probe)
+    y = W.expert_rows(probe.R, probe.H)
+    t0 = time.perf_counter()
+    oracle_step(probe, inp, y)
+    per_token = (time.perf_counter() - t0) / probe.T
+    T_s = int(max(1, min(wl.T, step_seconds / max(per_token, 1e-9))))
+    sample = wl.shrink(T_s) if T_s < wl.T else wl
+    inp = W.make(sample)
+    y = W.expert_rows(sample.R, sample.H)
+    n_live = int((inp["topk_idx"] >= 0).sum())
+    return sample, inp, y, sum(algorithmic_bytes(sample, n_live).values())
+
+
+def time_oracle(wl: W.Workload, budget_s: float = 12.0, min_reps: int = 3) -> dict:
+    """The oracle, as it stands (single-threaded C), on a bounded sample."""
+    sample, inp, y, total_bytes = oracle_sample(wl, step_seconds=min(1.0, budget_s / 4))
+    times = []
+    while len(times) < min_reps or sum(times) < budget_s:
+        t0 = time.perf_counter()
+        oracle_step(sample, inp, y)
+        times.append(time.perf_counter() - t0)
+    per_step = statistics.median(times)
+    return dict(value=round(total_bytes / per_step / 1e9, 4), unit="GB/s", cores=1, kind="oracle",
+                sample=f"first {sample.T} of {wl.T} tokens of the {wl.name} workload, whole "
+                       f"layout+dispatch+combine step, {len(times)} steps, median {per_step * 1e3:.1f} ms/step, "
+                       f"single-threaded C oracle",
+                seconds=round(sum(times), 2), host_cpus=os.cpu_count())
+
+
+# ------------------------------------------------------------------- GPU
+
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    import combine_ep_get_04_gb300 as ep
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    wl = W.WORKLOADS[args.workload]
+    inp = W.make(wl)
+    cap = wl.capacity if wl.mode == W.CAPACITY else None
+    plan = ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, cap, fp8=wl.fp8)
+    idx_d = torch.from_numpy(inp["topk_idx"]).cuda()
+    x_d = torch.from_numpy(inp["x"].view(np.int16)).cuda().view(torch.bfloat16)
+    w_d = torch.from_numpy(inp["topk_w"]).cuda()
+    gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
+    y_d = torch.randn((plan.R, wl.H), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    n_live = int((inp["topk_idx"] >= 0).sum())
+    nbytes = algorithmic_bytes(wl, n_live)
+    step_bytes = sum(nbytes.values())
+    layout_launches = 2 if plan.workspace_bytes > 0 else 1
+    launches_per_step = layout_launches + 2
+
+    def do_layout():
+        plan.layout(idx_d, clear_flags=False)
+
+    def do_dispatch():
+        plan.dispatch(x_d)
+
+    def do_combine():
+        plan.combine(y_d, w_d)
+
+    def do_step():
+        do_layout()
+        do_dispatch()
+        do_combine()
+
+    plan.layout_out.err_flags.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            do_step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    graphs = {"step": capture(do_step), "layout": capture(do_layout), "dispatch": capture(do_dispatch),
+              "combine": capture(do_combine)}
+    stream = torch.cuda.current_stream()
+
+    def timed(g, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        return evs
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # bring the clocks up (~0.5 s of back-to-back steps), then the warm-up steps
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            graphs["step"].replay()
+        torch.cuda.synchronize()
+    timed(graphs["step"], args.warmup)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_evs = timed(graphs["step"], args.steps)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    step_ms = [a.elapsed_time(b) for a, b in step_evs]
+
+    # ---- per-kernel times, same flush discipline
+    reps = max(args.steps, 20)
+    per_kernel = {}
+    for name in ("layout", "dispatch", "combine"):
+        evs = timed(graphs[name], reps)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        per_kernel[name] = dict(us=round(statistics.median(ms) * 1e3, 3),
+                                us_mean=round(statistics.fmean(ms) * 1e3, 3))
+
+    # ---- e2e through the public API with host buffers
+    x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
+    w_h = torch.from_numpy(inp["topk_w"]).pin_memory()
+    out_h = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    h2d = x_h.numel() * 2 + idx_h.numel() * 4 + w_h.numel() * 4
+    d2h = out_h.numel() * 2
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        do_step()
+        out_h.copy_(plan.out, non_blocking=True)
+        b.record(stream)
+        if it >= args.warmup:
+            e2e_ms.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ms]
+    clocks = sampler.stop()
+
+    flags = int(plan.layout_out.err_flags.item())
+    if flags:
+        raise RuntimeError(f"device error flags set during the benchmark: {flags:#x}")
+
+    ms_mean = statistics.fmean(step_ms)
+    e2e_mean = statistics.fmean(e2e_ms)
+    vals = torch.tensor([ms_mean, e2e_mean, wall], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_mean, e2e_mean, wall = vals.tolist()
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peak, peak_kind = hbm_peak()
+    for name, r in per_kernel.items():
+        gbs = nbytes[name] / (r["us"] * 1e-6) / 1e9
+        r.update(bytes=nbytes[name], gbs=round(gbs, 1), frac_of_hbm=round(gbs / peak, 4))
+    dominant = max(("dispatch", "combine", "layout"), key=lambda n: per_kernel[n]["us"])
+    dk = per_kernel[dominant]
+    ach = nbytes[dominant] / (dk["us_mean"] * 1e-6) / 1e9
+    traffic = ncu_traffic(wl.name, dominant)
+    value = world * step_bytes / (ms_mean * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (e2e_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_mean, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8-e4m3+bf16" if wl.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
+                   "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
+                   "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
+                   "step_bytes": step_bytes, "l2": "flushed (512 MB write) before every timed step",
+                   "timing": "CUDA-graph replay of layout+dispatch+combine, CUDA events per step",
+                   "parallelism": f"replicas x{world}"},
+        "kernels": per_kernel,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": nbytes[dominant], "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_mean, 5),
+                "how": "pinned host x/topk_idx/topk_w -> device, 3 public-API calls, out -> host"},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = time_oracle(wl, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_reference(args, rank: int, world: int) -> dict | None:
+    """The reference arm: the CPU oracle on the same workload, each step a
+    bounded sample (rank 0 only; other ranks exit without work)."""
+    if rank != 0:
+        return None
+    wl = W.WORKLOADS[args.workload]
+    step_s = min(1.0, max(0.05, args.cpu_seconds * 5 / max(1, args.steps + args.warmup)))
+    sample, inp, y, total_bytes = oracle_sample(wl, step_seconds=step_s)
+    times = []
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle_step(sample, inp, y)
+        if it >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = statistics.fmean(times)
+    value = total_bytes / per_step / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3+bf16" if wl.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
+                   "top_k": wl.k, "partitions": wl.P, "sample_tokens": sample.T},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {sample.T} of {wl.T} tokens of the {wl.name} workload per step, "
+                                   f"single-threaded C oracle", "host_cpus": os.cpu_count()},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=tuple(W.WORKLOADS), default="decode")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("for --gpus > 1 launch with torch.distributed.run (one rank per GPU)")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,337 @@
+// dispatch.cu -- copy each token's hidden row to every receive row it is
+// routed to (ep_dispatch), as a bf16 bit copy or with a fused per-128-channel
+// amax / FP8 e4m3 cast.
+//
+// Prior art: "Pipeline direct NVLink dispatch with triple-buffered prefetch"
+// (DeepEP PR #693), Summary: each dispatch warp stages tokens through shared
+// memory with the TMA engine; three buffers hold the token whose stores are
+// still in flight, the token being sent and the token being prefetched, and
+// the oldest buffer is recycled once at most one store group is outstanding.
+// Here the destination is this GPU's own HBM, so the same pipeline becomes:
+//   bulk copy global->shared of the next unit (mbarrier completion) while the
+//   k bulk copies shared->global of earlier units drain (bulk groups).
+// A unit is a token row, or a slice of it when there are few tokens, so the
+// grid covers every SM.  Each row of x is read from HBM once and written k
+// times; no thread touches the payload on the bf16 path.
+#include "ep_device.cuh"
+#include "ep_kernels.h"
+
+namespace ep {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Bf16Args {
+    const unsigned char* x;
+    const int32_t* slot_of;
+    const float* topk_w;
+    unsigned char* recv;
+    float* recv_w;
+    uint32_t* err_flags;
+    int64_t R;             // receive rows
+    int64_t units;         // T * slices
+    int64_t row_bytes;     // H * 2
+    int slices;            // units per token row
+    int k;
+    uint32_t slice_bytes;  // row_bytes / slices, multiple of 16
+    uint32_t stage_stride; // slice_bytes rounded up to 128
+};
+
+// One warp per CTA.  Lane 0 issues the loads; lane j issues the store of copy j.
+template <int NS, int LA>
+__global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
+    static_assert(LA >= 1 && LA <= NS - 1, "lookahead must leave a stage for the stores");
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* stages = smem + 128;
+    const int lane = threadIdx.x;
+    const int64_t first = blockIdx.x;
+    if (first >= a.units) return;
+    const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    auto issue_load = [&](int64_t i) {
+        const int64_t u = first + i * gridDim.x;
+        const int64_t t = u / a.slices;
+        const int sl = (int)(u - t * a.slices);
+        const int s = (int)(i % NS);
+        mbar_arrive_expect_tx(&bars[s], a.slice_bytes);
+        bulk_load(stages + (size_t)s * a.stage_stride,
+                  a.x + t * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes, &bars[s]);
+    };
+
+    if (lane == 0) {
+        for (int64_t i = 0; i < LA && i < n_mine; ++i) issue_load(i);
+    }
+
+    bool ok = true;
+    int64_t i = 0;
+    for (; i < n_mine; ++i) {
+        const int64_t u = first + i * gridDim.x;
+        const int64_t t = u / a.slices;
+        const int sl = (int)(u - t * a.slices);
+        const int s = (int)(i % NS);
+        // Stage (i+LA)%NS was last read by the stores of unit i+LA-NS; at most
+        // NS-LA-1 younger store groups may still be reading their stages.
+        if (i + LA < n_mine) {
+            bulk_wait_read<NS - LA - 1>();
+            __syncwarp();
+            if (lane == 0) issue_load(i + LA);
+        }
+        int32_t slot = -1;
+        float w = 0.f;
+        if (lane < a.k) {
+            slot = __ldg(a.slot_of + t * a.k + lane);
+            if (slot < -1 || slot >= a.R) {
+                if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
+                slot = -1;
+            }
+            if (a.recv_w != nullptr && sl == 0 && slot >= 0) w = __ldg(a.topk_w + t * a.k + lane);
+        }
+        ok = __all_sync(kFull, mbar_wait(&bars[s], (uint32_t)((i / NS) & 1)));
+        if (!ok) break;
+        if (slot >= 0) {
+            bulk_store(a.recv + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes,
+                       stages + (size_t)s * a.stage_stride, a.slice_bytes);
+            if (a.recv_w != nullptr && sl == 0) a.recv_w[slot] = w;
+        }
+        bulk_commit();
+    }
+    bulk_wait_all();
+    if (!ok) {
+        // Loads still in flight target this CTA's shared memory: let them land
+        // (each wait bounded) before the CTA exits.
+        if (lane == 0) {
+            for (int64_t r = i; r < i + LA && r < n_mine; ++r) {
+                (void)mbar_wait(&bars[r % NS], (uint32_t)((r / NS) & 1));
+            }
+            if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+        }
+    }
+}
+
+struct Fp8Args {
+    const unsigned char* x;
+    const int32_t* slot_of;
+    const float* topk_w;
+    unsigned char* recv;     // e4m3 [R, H]
+    float* recv_s;           // [R, H/128]
+    float* recv_w;
+    uint32_t* err_flags;
+    int64_t R;               // receive rows
+    int64_t units;           // T * slices
+    int H;
+    int nb;                  // H / 128
+    int slices;
+    int nblk;                // 128-channel blocks per unit
+    int k;
+    int scale_bulk;          // scales stored with a bulk copy (16-byte granular)
+    uint32_t in_stride;      // bytes per input stage (nblk*256, multiple of 128)
+    uint32_t out_stride;     // bytes per output stage: nblk*128 q + nblk*4 scales, rounded to 128
+};
+
+constexpr int kFp8Warps = 8;
+constexpr int kFp8Threads = kFp8Warps * 32;
+constexpr int kFp8OutStages = 2;
+
+// Warp 0 issues loads (lane 0) and the k stores (lane j); all warps quantise.
+template <int NS>
+__global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* in_st = smem + 128;
+    unsigned char* out_st = in_st + (size_t)NS * a.in_stride;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t first = blockIdx.x;
+    if (first >= a.units) return;
+    const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
+    const uint32_t in_bytes = (uint32_t)a.nblk * 256u;
+    const uint32_t q_bytes = (uint32_t)a.nblk * 128u;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue_load = [&](int64_t i) {
+        const int64_t u = first + i * gridDim.x;
+        const int64_t t = u / a.slices;
+        const int sl = (int)(u - t * a.slices);
+        const int s = (int)(i % NS);
+        mbar_arrive_expect_tx(&bars[s], in_bytes);
+        bulk_load(in_st + (size_t)s * a.in_stride,
+                  a.x + (t * a.H + (int64_t)sl * a.nblk * 128) * 2, in_bytes, &bars[s]);
+    };
+    if (tid == 0) {
+        for (int64_t i = 0; i < NS - 1 && i < n_mine; ++i) issue_load(i);
+    }
+
+    bool ok = true;
+    int64_t i = 0;
+    for (; i < n_mine; ++i) {
+        const int64_t u = first + i * gridDim.x;
+        const int64_t t = u / a.slices;
+        const int sl = (int)(u - t * a.slices);
+        const int s = (int)(i % NS);
+        unsigned char* ob = out_st + (size_t)(i % kFp8OutStages) * a.out_stride;
+        float* oscale = reinterpret_cast<float*>(ob + q_bytes);
+
+        // Output stage i%2 was read by the stores of unit i-2.
+        if (warp == 0 && i >= kFp8OutStages) bulk_wait_read<kFp8OutStages - 1>();
+        __syncthreads();
+        // Input stage (i+NS-1)%NS was last read while quantising unit i-1.
+        if (tid == 0 && i + NS - 1 < n_mine) issue_load(i + NS - 1);
+
+        int32_t slot = -1;
+        float w = 0.f;
+        if (warp == 0 && lane < a.k) {
+            slot = __ldg(a.slot_of + t * a.k + lane);
+            if (slot < -1 || slot >= a.R) {
+                if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
+                slot = -1;
+            }
+            if (a.recv_w != nullptr && sl == 0 && slot >= 0) w = __ldg(a.topk_w + t * a.k + lane);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[s], (uint32_t)((i / NS) & 1))) != 0;
+        if (!ok) break;
+
+        const unsigned char* ib = in_st + (size_t)s * a.in_stride;
+        for (int b = warp; b < a.nblk; b += kFp8Warps) {
+            const uint2 v = *reinterpret_cast<const uint2*>(ib + b * 256 + lane * 8);
+            const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
+            float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
+            const float sc = __fdiv_rn(fmaxf(m, 1e-4f), 448.0f);
+            const uint32_t q01 = pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
+            const uint32_t q23 = pack_e4m3x2(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
+            *reinterpret_cast<uint32_t*>(ob + b * 128 + lane * 4) = q01 | (q23 << 16);
+            if (lane == 0) oscale[b] = sc;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        if (warp == 0) {
+            if (slot >= 0) {
+                bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, ob, q_bytes);
+                float* sdst = a.recv_s + (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
+                if (a.scale_bulk) {
+                    bulk_store(sdst, oscale, (uint32_t)a.nblk * 4u);
+                } else {
+                    for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
+                }
+                if (a.recv_w != nullptr && sl == 0) a.recv_w[slot] = w;
+            }
+            bulk_commit();
+        }
+    }
+    if (warp == 0) bulk_wait_all();
+    if (!ok && tid == 0) {
+        for (int64_t r = i; r < i + NS - 1 && r < n_mine; ++r) {
+            (void)mbar_wait(&bars[r % NS], (uint32_t)((r / NS) & 1));
+        }
+        if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+    }
+}
+
+// Number of slices a row of n granules is cut into: the smallest divisor d of
+// n whose slices hold at most max_per granules and give T*d >= want units;
+// slices never drop below min_per granules once one size fits.
+int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t want) {
+    int best = 0;
+    for (int64_t d = 1; d <= n; ++d) {
+        if (n % d) continue;
+        const int64_t per = n / d;
+        if (per > max_per) continue;
+        if (best && per < min_per) break;
+        best = (int)d;
+        if (T * d >= want) break;
+    }
+    return best ? best : (int)n;
+}
+
+}  // namespace
+
+constexpr int kBf16Stages = 4;
+constexpr int kBf16Lookahead = 2;
+constexpr int kFp8Stages = 3;
+
+cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStream_t stream) {
+    if (p.T == 0) return cudaSuccess;
+    Bf16Args a{};
+    a.x = static_cast<const unsigned char*>(p.x);
+    a.slot_of = p.slot_of;
+    a.topk_w = p.topk_w;
+    a.recv = static_cast<unsigned char*>(p.recv);
+    a.recv_w = p.recv_w;
+    a.err_flags = p.err_flags;
+    a.R = p.R;
+    a.row_bytes = (int64_t)p.H * 2;
+    a.k = p.k;
+    // Units of at most 16 KB, at least 1 KB, enough of them for ~4 per SM.
+    const int64_t vec16 = a.row_bytes / 16;
+    a.slices = pick_slices(p.T, vec16, 1024, 64, 4LL * num_sms);
+    a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+    a.stage_stride = (a.slice_bytes + 127u) & ~127u;
+    a.units = (int64_t)p.T * a.slices;
+    const size_t smem = 128 + (size_t)kBf16Stages * a.stage_stride;
+    auto kern = dispatch_bf16_kernel<kBf16Stages, kBf16Lookahead>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms * per_sm;
+    if (grid > a.units) grid = a.units;
+    kern<<<(unsigned)grid, 32, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream_t stream) {
+    if (p.T == 0) return cudaSuccess;
+    Fp8Args a{};
+    a.x = static_cast<const unsigned char*>(p.x);
+    a.slot_of = p.slot_of;
+    a.topk_w = p.topk_w;
+    a.recv = static_cast<unsigned char*>(p.recv);
+    a.recv_s = p.recv_scales;
+    a.recv_w = p.recv_w;
+    a.err_flags = p.err_flags;
+    a.R = p.R;
+    a.H = p.H;
+    a.nb = p.H / 128;
+    a.k = p.k;
+    // Units of at most 64 blocks (16 KB of bf16), enough for ~4 per SM.
+    a.slices = pick_slices(p.T, a.nb, 64, 2, 4LL * num_sms);
+    a.nblk = a.nb / a.slices;
+    a.scale_bulk = (a.nb % 4 == 0) && (a.nblk % 4 == 0);
+    a.in_stride = (uint32_t)a.nblk * 256u;
+    a.out_stride = ((uint32_t)a.nblk * 132u + 127u) & ~127u;
+    a.units = (int64_t)p.T * a.slices;
+    const size_t smem = 128 + (size_t)kFp8Stages * a.in_stride + (size_t)kFp8OutStages * a.out_stride;
+    auto kern = dispatch_fp8_kernel<kFp8Stages>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFp8Threads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms * per_sm;
+    if (grid > a.units) grid = a.units;
+    kern<<<(unsigned)grid, kFp8Threads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,72 @@
+// ep_kernels.h -- host-side launchers of the dispatch / combine kernels and
+// their parameter blocks (internal to the library; the public C ABI is
+// include/ep.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ep {
+
+// ----------------------------------------------------------------- layout
+
+constexpr int64_t kLayoutChunk = 1024;   // entries ranked by one CTA
+constexpr int64_t kLayoutSmallN = 4096;  // up to this many entries: one launch, no workspace
+
+struct LayoutParams {
+    const int32_t* topk_idx;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* part_counts;
+    int32_t* part_offsets;
+    int32_t* slot_of;
+    int32_t* src_token;
+    int32_t* src_k;
+    int32_t* hist;        // [num_chunks][E] workspace, or nullptr for the one-launch path
+    uint32_t* err_flags;  // may be nullptr
+    int64_t N;            // T * k
+    int64_t R;            // receive rows
+    int64_t chunk;        // set by launch_layout
+    int num_chunks;       // set by launch_layout
+    int E, P, k, mode, cap;
+};
+
+int64_t layout_num_chunks(int64_t N);
+bool layout_uses_workspace(int64_t N);
+size_t layout_workspace_bytes(int64_t N, int E);
+size_t layout_rank_smem_bytes(int E);
+cudaError_t launch_layout(const LayoutParams& p, int num_sms, cudaStream_t stream);
+
+// --------------------------------------------------------------- dispatch
+
+struct DispatchParams {
+    const void* x;          // bf16 [T, H]
+    const float* topk_w;    // [T, k] or nullptr
+    const int32_t* slot_of; // [T, k]
+    void* recv;             // bf16 or e4m3 [R, H]
+    float* recv_scales;     // [R, H/128] (fp8)
+    float* recv_w;          // [R] or nullptr
+    uint32_t* err_flags;    // may be nullptr
+    int64_t R;              // receive rows
+    int T, H, k;
+};
+
+cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- combine
+
+struct CombineParams {
+    const void* y;          // bf16 [R, H]
+    const float* topk_w;    // [T, k]
+    const int32_t* slot_of; // [T, k]
+    void* out;              // bf16 [T, H]
+    uint32_t* err_flags;    // may be nullptr
+    int64_t R;              // rows of y
+    int T, H, k;
+};
+
+cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t stream);
+
+}  // namespace ep

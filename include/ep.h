@@ -1,0 +1,203 @@
+/*
+ * ep.h -- C ABI of a single-GPU MoE token dispatch / combine library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the DeepEP pages this library is built from:
+ *  - "Redundant atomics in internode_ll" (DeepEP issue #282), the quoted
+ *    low-latency dispatch excerpt: a token count per expert, and expert e
+ *    living on partition e / (experts per partition) as local expert
+ *    e % (experts per partition).
+ *  - "Reasons for not calling NVSHMEM public APIs?" (DeepEP issue #18), the
+ *    answer on low-latency mode: data for one expert keeps its order.
+ *  - "Pipeline direct NVLink dispatch with triple-buffered prefetch" (DeepEP
+ *    PR #693), Summary: each token carries hidden data, scale factors,
+ *    metadata and routing; the next token is prefetched while earlier stores
+ *    drain.  Validation table: dispatch and combine are the measured pair.
+ * Here all experts live in one GPU's HBM; partitions are logical only.
+ *
+ * Conventions for every entry point
+ *  - Device pointers are raw CUDA device addresses.  The caller allocates and
+ *    frees every buffer (including the layout workspace); the library never
+ *    allocates, frees or synchronises.
+ *  - All work is enqueued on `stream` (NULL = the legacy default stream).  A
+ *    return of EP_OK means the work was enqueued; results are ready once the
+ *    stream reaches that point.  Calls are stateless and thread-safe.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns EP_ERR_INVALID_ARG (unsupported sizes EP_ERR_UNSUPPORTED)
+ *    with nothing enqueued.  A failed launch returns EP_ERR_CUDA.  The text of
+ *    the last failure on the calling thread is available from ep_last_error().
+ *  - Conditions found on the device never trap: they are OR-ed into the
+ *    caller's 32-bit `err_flags` word (EP_ERRF_*), which the caller clears and
+ *    reads back.  `err_flags` may be NULL, in which case they are dropped.
+ *  - A buffer of zero elements may be passed as NULL.
+ *  - Element types: bf16 is stored as 16-bit IEEE bfloat16; fp8 as one byte of
+ *    OCP e4m3 ("e4m3fn": bias 7, max 448, no infinities); f32 / i32 native.
+ *  - All arrays are dense and row-major.
+ */
+#ifndef EP_GB300_H_
+#define EP_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *ep_stream_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, bad shape       */
+    EP_ERR_UNSUPPORTED = 2,   /* valid but beyond this build's limits, or no
+                                 sm_103 device current                        */
+    EP_ERR_CUDA = 3           /* a CUDA runtime call or launch failed         */
+} ep_status_t;
+
+typedef enum {
+    EP_LAYOUT_PACKED = 0,     /* R = T*k rows, expert e owns rows
+                                 [offsets[e], offsets[e+1])                   */
+    EP_LAYOUT_CAPACITY = 1    /* R = E*capacity rows, expert e owns rows
+                                 [e*capacity, (e+1)*capacity)                 */
+} ep_layout_mode_t;
+
+/* Payload format of ep_dispatch. */
+typedef enum {
+    EP_PAYLOAD_BF16 = 0,      /* recv is bf16 [R, H], a bit copy of x         */
+    EP_PAYLOAD_FP8_E4M3 = 1   /* recv is e4m3 [R, H] plus f32 scales [R, H/128] */
+} ep_payload_t;
+
+/* Bits of the device error word. */
+enum {
+    EP_ERRF_BAD_EXPERT = 1u,  /* a topk_idx entry outside [-1, E); treated as -1 */
+    EP_ERRF_CAPACITY = 2u,    /* capacity mode dropped at least one copy      */
+    EP_ERRF_TIMEOUT = 4u,     /* an internal bounded wait ran out; outputs of
+                                 that call are incomplete                     */
+    EP_ERRF_BAD_SLOT = 8u     /* a slot_of entry >= R (or < -1); that copy was
+                                 skipped                                      */
+};
+
+/* Limits of this build. */
+#define EP_MAX_EXPERTS 1024
+#define EP_MAX_TOPK 32
+
+typedef struct {
+    int32_t T;                /* tokens, >= 0                                  */
+    int32_t H;                /* hidden channels, > 0, multiple of 8 (of 128
+                                 for fp8 payloads)                             */
+    int32_t E;                /* experts, 1..EP_MAX_EXPERTS                    */
+    int32_t k;                /* experts per token, 1..min(E, EP_MAX_TOPK)     */
+    int32_t num_partitions;   /* P >= 1, divides E; partition p holds experts
+                                 [p*E/P, (p+1)*E/P)                            */
+    int32_t mode;             /* ep_layout_mode_t                              */
+    int32_t capacity;         /* rows per expert, >= 1 in capacity mode        */
+} ep_shape_t;
+
+/* Rows R of the receive buffer for this shape; -1 if the shape is invalid. */
+EP_API int64_t ep_recv_rows(const ep_shape_t *shape);
+
+/* Bytes of device workspace ep_get_layout needs for this shape (may be 0);
+ * (size_t)-1 if the shape is invalid. */
+EP_API size_t ep_layout_workspace_bytes(const ep_shape_t *shape);
+
+/*
+ * ep_get_layout -- turn top-k routing into the per-expert layout.
+ *
+ * In:  topk_idx   i32 [T, k]  expert of copy (t, j); -1 = masked slot.
+ * Out: counts       i32 [E]    copies routed to each expert (true demand,
+ *                              also in capacity mode).
+ *      offsets      i32 [E+1]  exclusive prefix sum of counts.
+ *      part_counts  i32 [P]    counts summed over each partition.
+ *      part_offsets i32 [P+1]  exclusive prefix sum of part_counts.
+ *      slot_of      i32 [T, k] receive row of copy (t, j); -1 if masked or
+ *                              dropped for capacity.
+ *      src_token    i32 [R]    token of each receive row; -1 if the row holds
+ *                              no copy.
+ *      src_k        i32 [R]    top-k position j of each receive row; -1 if
+ *                              the row holds no copy.
+ * Order: rows of one expert hold its copies in increasing (t, j), so the
+ * result is deterministic and equals a stable sort of the flattened ids.
+ *   packed:   slot = offsets[e] + rank(t, j),
+ *   capacity: slot = e*capacity + rank if rank < capacity, else dropped
+ *             (EP_ERRF_CAPACITY),
+ * rank(t, j) = number of copies (t', j') < (t, j) routed to the same expert.
+ * workspace: device buffer of ep_layout_workspace_bytes(shape) bytes, owned
+ * by the caller, contents on entry ignored; NULL allowed when that is 0.
+ * err_flags: EP_ERRF_BAD_EXPERT, EP_ERRF_CAPACITY.
+ */
+EP_API ep_status_t ep_get_layout(const ep_shape_t *shape, const int32_t *topk_idx,
+                          int32_t *counts, int32_t *offsets,
+                          int32_t *part_counts, int32_t *part_offsets,
+                          int32_t *slot_of, int32_t *src_token, int32_t *src_k,
+                          void *workspace, size_t workspace_bytes,
+                          uint32_t *err_flags, ep_stream_t stream);
+
+/*
+ * ep_dispatch -- copy every token's hidden row to each receive row it is
+ * routed to (slot_of from ep_get_layout; R = ep_recv_rows(shape)).
+ *
+ * In:  x        bf16 [T, H], 16-byte aligned.
+ *      topk_w   f32 [T, k] routing weights, or NULL.
+ *      slot_of  i32 [T, k] receive row of each copy, -1 = none; each
+ *               non-negative value should appear at most once (rows written
+ *               twice end up with either copy); values outside [-1, R) are
+ *               skipped and flagged EP_ERRF_BAD_SLOT.
+ * Out: recv     EP_PAYLOAD_BF16:     bf16 [R, H]: recv[slot_of[t,j]] = x[t].
+ *               EP_PAYLOAD_FP8_E4M3: e4m3 [R, H]; per token t and channel
+ *               block b of 128: s = max(amax, 1e-4) / 448 (fp32, round to
+ *               nearest), q = e4m3(x / s) (fp32 division rounded to nearest,
+ *               then nearest e4m3, ties to even, saturating at +-448).
+ *               16-byte aligned.
+ *      recv_scales f32 [R, H/128] (fp8 only, else ignored): s of each block,
+ *               16-byte aligned.
+ *      recv_w   f32 [R] or NULL: recv_w[slot_of[t,j]] = topk_w[t,j]
+ *               (needs topk_w).
+ * Rows of recv / recv_scales / recv_w that receive no copy are not written.
+ * err_flags: EP_ERRF_TIMEOUT, EP_ERRF_BAD_SLOT.
+ */
+EP_API ep_status_t ep_dispatch(const ep_shape_t *shape, const void *x,
+                        const float *topk_w, const int32_t *slot_of,
+                        int32_t payload, void *recv, float *recv_scales,
+                        float *recv_w, uint32_t *err_flags, ep_stream_t stream);
+
+/*
+ * ep_combine -- weighted top-k reduce of expert outputs back to token order.
+ *
+ * In:  y        bf16 [R, H] expert outputs in the receive layout, 16-byte
+ *               aligned.
+ *      topk_w   f32 [T, k].
+ *      slot_of  i32 [T, k] from ep_get_layout (-1 = skipped; values outside
+ *               [-1, R) are skipped and flagged EP_ERRF_BAD_SLOT).
+ * Out: out      bf16 [T, H], 16-byte aligned:
+ *               out[t] = bf16( sum_{j: slot_of[t,j] >= 0} topk_w[t,j] * y[slot_of[t,j]] ),
+ *               accumulated in fp32 in increasing j from 0 (each product and
+ *               sum rounded to nearest), rounded once to bf16 (nearest even).
+ *               A token with no valid slot gets 0.
+ * err_flags: EP_ERRF_BAD_SLOT.
+ */
+EP_API ep_status_t ep_combine(const ep_shape_t *shape, const void *y,
+                       const float *topk_w, const int32_t *slot_of, void *out,
+                       uint32_t *err_flags, ep_stream_t stream);
+
+/* Static description of a status code. */
+EP_API const char *ep_status_string(ep_status_t status);
+
+/* Detail of the last non-EP_OK status returned on the calling thread
+ * ("" if none).  The pointer stays valid until the next call on this thread. */
+EP_API const char *ep_last_error(void);
+
+/* ABI version of this library (major * 100 + minor). */
+EP_API int32_t ep_abi_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* EP_GB300_H_ */

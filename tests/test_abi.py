@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads and exports every symbol include/ep.h
+declares; host-side argument checks reject bad calls before any CUDA call.
+
+Runs without a GPU: only entry points that return before touching the device
+are called.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_ep_get_04_gb300 as ep
+from combine_ep_get_04_gb300 import _lib
+from combine_ep_get_04_gb300 import build as epbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    epbuild.build()
+    return ep.load()
+
+
+def declared_symbols() -> list[str]:
+    text = open(os.path.join(ROOT, "include", "ep.h")).read()
+    return re.findall(r"EP_API\s+[\w\s\*]*?\b(ep_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(declared_symbols()) == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # the ELF dynamic symbol table, independently of ctypes
+    out = os.popen(f"nm -D --defined-only {ep.library_path()}").read()
+    exported = set(re.findall(r" T (ep_\w+)", out))
+    assert set(declared_symbols()) <= exported
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.ep_abi_version() == 100
+    assert lib.ep_status_string(0) == b"ok"
+    assert lib.ep_status_string(1) == b"invalid argument"
+
+
+def test_rows_and_workspace(lib):
+    s = ep.make_shape(128, 7168, 256, 8, 32, capacity=128)
+    assert ep.recv_rows(s) == 256 * 128
+    assert ep.layout_workspace_bytes(s) == 0            # 1024 entries: one launch, no workspace
+    s = ep.make_shape(16384, 4096, 128, 8, 8)
+    assert ep.recv_rows(s) == 16384 * 8
+    assert ep.layout_workspace_bytes(s) == 128 * 128 * 4  # 128 chunks x 128 experts x i32
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(H=0), dict(H=12), dict(E=0), dict(k=0), dict(k=17), dict(num_partitions=3),
+    dict(mode=2), dict(mode=1, capacity=0)])
+def test_bad_shapes_rejected(lib, bad):
+    f = dict(T=4, H=64, E=16, k=4, num_partitions=1, mode=0, capacity=0)
+    f.update(bad)
+    s = _lib.Shape(**f)
+    assert lib.ep_recv_rows(ctypes.byref(s)) == -1
+    st = lib.ep_get_layout(ctypes.byref(s), *([None] * 9), 0, None, None)
+    assert st == _lib.EP_ERR_INVALID_ARG
+    assert lib.ep_last_error()
+
+
+def test_unsupported_sizes(lib):
+    s = _lib.Shape(4, 64, 2048, 4, 1, 0, 0)
+    assert lib.ep_dispatch(ctypes.byref(s), *([None] * 3), 0, *([None] * 5)) == _lib.EP_ERR_UNSUPPORTED
+    s = _lib.Shape(4, 64, 64, 33, 1, 0, 0)
+    assert lib.ep_combine(ctypes.byref(s), *([None] * 6)) == _lib.EP_ERR_UNSUPPORTED
+
+
+def test_host_checks_before_device(lib):
+    s = _lib.Shape(4, 64, 16, 4, 1, 0, 0)
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: rejected on the host
+    # null pointers
+    assert lib.ep_dispatch(ctypes.byref(s), None, None, fake, 0, fake, None, None, None, None) == 1
+    # misaligned x / recv / y / out
+    odd = ctypes.c_void_p(0x10002)
+    assert lib.ep_dispatch(ctypes.byref(s), odd, None, fake, 0, fake, None, None, None, None) == 1
+    assert lib.ep_dispatch(ctypes.byref(s), fake, None, fake, 0, odd, None, None, None, None) == 1
+    assert lib.ep_combine(ctypes.byref(s), odd, fake, fake, fake, None, None) == 1
+    assert lib.ep_combine(ctypes.byref(s), fake, fake, fake, odd, None, None) == 1
+    # fp8 needs H % 128 == 0 and aligned scales
+    assert lib.ep_dispatch(ctypes.byref(s), fake, None, fake, 1, fake, fake, None, None, None) == 1
+    s128 = _lib.Shape(4, 128, 16, 4, 1, 0, 0)
+    assert lib.ep_dispatch(ctypes.byref(s128), fake, None, fake, 1, fake, None, None, None, None) == 1
+    assert lib.ep_dispatch(ctypes.byref(s128), fake, None, fake, 1, fake, odd, None, None, None) == 1
+    # unknown payload, recv_w without topk_w
+    assert lib.ep_dispatch(ctypes.byref(s), fake, None, fake, 7, fake, None, None, None, None) == 1
+    assert lib.ep_dispatch(ctypes.byref(s), fake, None, fake, 0, fake, None, fake, None, None) == 1
+    # layout: workspace too small for a large shape
+    big = _lib.Shape(8192, 64, 16, 8, 1, 0, 0)
+    assert lib.ep_get_layout(ctypes.byref(big), *([fake] * 8), None, 0, None, None) == 1
+    assert b"workspace" in lib.ep_last_error()
+    # T == 0 is a no-op for dispatch / combine
+    z = _lib.Shape(0, 64, 16, 4, 1, 0, 0)
+    assert lib.ep_dispatch(ctypes.byref(z), *([None] * 3), 0, *([None] * 5)) == 0
+    assert lib.ep_combine(ctypes.byref(z), *([None] * 6)) == 0
+
+
+def test_product_path_does_not_use_the_oracle():
+    """The package never imports the oracle or any CPU fallback."""
+    pkg = os.path.join(ROOT, "combine_ep_get_04_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f

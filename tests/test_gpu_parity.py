@@ -1,0 +1,374 @@
+"""GPU path vs the CPU oracle, through the C ABI (via the ctypes binding).
+
+Bar: layout, indices, bf16 receive rows and the fp8 payload + scales are
+bit-exact; combine is within |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| (bf16).
+Sizes: every workload at full size (whole outputs where the oracle is fast,
+sampled tokens plus size-independent properties where the inputs are over a
+gigabyte), shrunken workloads, random shapes crossing every tile and chunk
+boundary, and the degenerate cases (T = 0, T = 1, k = 1, k = E, all copies to
+one expert, capacity overflow, bad ids, all-zero blocks).
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_get_04_gb300 as ep
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+RTOL = ATOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    ep.load()
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bf16_dev(bits: np.ndarray) -> torch.Tensor:
+    return dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def plan_for(wl: W.Workload, with_weights=False) -> ep.Plan:
+    cap = wl.capacity if wl.mode == W.CAPACITY else None
+    return ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, cap, fp8=wl.fp8, with_weights=with_weights)
+
+
+def oracle_layout(wl: W.Workload, idx: np.ndarray) -> dict:
+    mode = oracle.CAPACITY if wl.mode == W.CAPACITY else oracle.PACKED
+    return oracle.layout(idx, wl.E, wl.P, mode, wl.capacity)
+
+
+def gpu_layout(plan: ep.Plan, idx: np.ndarray) -> dict:
+    L = plan.layout(dev(idx))
+    torch.cuda.synchronize()
+    out = {k: getattr(L, k).cpu().numpy() for k in
+           ("counts", "offsets", "part_counts", "part_offsets", "slot_of", "src_token", "src_k")}
+    out["err"] = int(L.err_flags.cpu().numpy().view(np.uint32)[0])
+    return out
+
+
+def assert_layout_equal(g: dict, o: dict):
+    for key in ("counts", "offsets", "part_counts", "part_offsets", "slot_of", "src_token", "src_k"):
+        np.testing.assert_array_equal(g[key], o[key], err_msg=key)
+    assert g["err"] == o["err"]
+
+
+def assert_combine_close(g_bits: np.ndarray, o_bits: np.ndarray):
+    g = oracle.bf16_to_f32(g_bits).astype(np.float64)
+    o = oracle.bf16_to_f32(o_bits).astype(np.float64)
+    bad = np.abs(g - o) > ATOL + RTOL * np.abs(o)
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance, max |diff| {np.abs(g - o).max()}"
+
+
+# ------------------------------------------------------------------ layout
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_layout_workloads_full_size(name):
+    d = W.make(name)
+    wl = d["wl"]
+    assert_layout_equal(gpu_layout(plan_for(wl), d["topk_idx"]), oracle_layout(wl, d["topk_idx"]))
+
+
+LAYOUT_FUZZ = [
+    # (T, E, k, P, capacity or None, mask_frac, duplicates allowed)
+    (1, 1, 1, 1, None, 0.0, False), (1, 16, 16, 4, None, 0.0, False), (3, 5, 2, 1, 1, 0.2, True),
+    (31, 7, 1, 7, None, 0.0, False), (33, 64, 1, 8, 2, 0.0, False), (128, 256, 8, 32, 128, 0.0, False),
+    (255, 9, 4, 3, None, 0.1, True), (256, 1024, 4, 16, None, 0.0, False), (1023, 2, 1, 1, None, 0.0, False),
+    (512, 2, 2, 2, None, 0.0, False), (1025, 300, 4, 4, 8, 0.05, False), (2048, 128, 2, 8, 16, 0.0, False),
+    (4097, 64, 1, 1, None, 0.3, True), (1500, 33, 3, 3, None, 0.0, True), (3000, 512, 8, 64, 40, 0.0, False),
+    (9000, 1024, 32, 8, None, 0.01, False), (20001, 96, 6, 12, 1200, 0.0, False), (700, 1, 1, 1, 500, 0.0, False),
+]
+
+
+@pytest.mark.parametrize("T,E,k,P,cap,mask,dup", LAYOUT_FUZZ)
+def test_layout_fuzz(T, E, k, P, cap, mask, dup):
+    rng = np.random.default_rng(T * 7919 + E * 31 + k)
+    if dup:
+        idx = rng.integers(0, E, size=(T, k))
+    else:
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :k]
+    idx = idx.astype(np.int32)
+    idx[rng.random((T, k)) < mask] = -1
+    wl = W.Workload("fuzz", T=T, H=8, E=E, k=k, P=P, routing="uniform", fp8=False,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    assert_layout_equal(gpu_layout(plan_for(wl), idx), oracle_layout(wl, idx))
+
+
+def test_layout_all_copies_to_one_expert_and_overflow():
+    T, E, k = 5000, 64, 1
+    idx = np.full((T, k), 37, np.int32)
+    for cap in (None, 100):
+        wl = W.Workload("one", T=T, H=8, E=E, k=k, P=8, routing="uniform", fp8=False,
+                        mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+        g = gpu_layout(plan_for(wl), idx)
+        o = oracle_layout(wl, idx)
+        assert_layout_equal(g, o)
+        assert bool(g["err"] & ep.ERRF_CAPACITY) == (cap is not None)
+
+
+def test_layout_bad_ids_flagged():
+    idx = np.array([[0, 16], [-7, 3], [15, -1], [2, 99]], np.int32)
+    wl = W.Workload("bad", T=4, H=8, E=16, k=2, P=4, routing="uniform", fp8=False)
+    g = gpu_layout(plan_for(wl), idx)
+    assert_layout_equal(g, oracle_layout(wl, idx))
+    assert g["err"] == ep.ERRF_BAD_EXPERT
+    big = np.random.default_rng(0).integers(-3, 20, size=(6000, 2)).astype(np.int32)
+    wl = W.Workload("bad2", T=6000, H=8, E=16, k=2, P=1, routing="uniform", fp8=False)
+    assert_layout_equal(gpu_layout(plan_for(wl), big), oracle_layout(wl, big))
+
+
+def test_layout_empty():
+    for cap in (None, 3):
+        wl = W.Workload("empty", T=0, H=8, E=8, k=2, P=2, routing="uniform", fp8=False,
+                        mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+        idx = np.zeros((0, 2), np.int32)
+        assert_layout_equal(gpu_layout(plan_for(wl), idx), oracle_layout(wl, idx))
+
+
+def test_layout_is_deterministic_and_on_any_stream():
+    d = W.make("skewed")
+    wl = d["wl"]
+    plan = plan_for(wl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = gpu_layout(plan, d["topk_idx"])
+    b = gpu_layout(plan, d["topk_idx"])
+    assert_layout_equal(a, b)
+
+
+# -------------------------------------------------------------- bf16 dispatch
+
+def _dispatch_bf16_case(wl: W.Workload, idx, x, w, sentinel=0x7FBF):
+    plan = plan_for(wl, with_weights=True)
+    plan.recv.view(torch.int16).fill_(sentinel)
+    plan.recv_w.fill_(-1.0)
+    plan.layout(dev(idx))
+    recv, _, recv_w = plan.dispatch(bf16_dev(x), dev(w))
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, idx)
+    o_recv = np.full((wl.R, wl.H), sentinel, np.uint16)
+    o_recv, o_w = oracle.dispatch_bf16(x, L["slot_of"], wl.R, w, recv=o_recv)
+    live = L["slot_of"][L["slot_of"] >= 0]
+    o_w_full = np.full(wl.R, -1.0, np.float32)
+    o_w_full[live] = o_w[live]
+    np.testing.assert_array_equal(bits(recv), o_recv)
+    np.testing.assert_array_equal(recv_w.cpu().numpy(), o_w_full)
+    assert int(plan.layout_out.err_flags.item()) & ep.ERRF_TIMEOUT == 0
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("prefill", None), ("grouped", 1536), ("prefill", 7)])
+def test_dispatch_bf16_workloads(name, T):
+    wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)
+    d = W.make(wl)
+    _dispatch_bf16_case(wl, d["topk_idx"], d["x"], d["topk_w"])
+
+
+@pytest.mark.parametrize("T,H,E,k,cap", [(1, 8, 4, 1, None), (3, 24, 4, 4, None), (200, 1032, 32, 6, None),
+                                         (17, 4104, 16, 3, 2), (64, 7168, 256, 8, 4), (1, 16384, 8, 8, None),
+                                         (5, 65536, 4, 2, None), (300, 136, 8, 8, None)])
+def test_dispatch_bf16_shapes(T, H, E, k, cap):
+    rng = np.random.default_rng(T + H)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < 0.1] = -1
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    w = rng.random((T, k)).astype(np.float32)
+    wl = W.Workload("s", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=False,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    _dispatch_bf16_case(wl, idx, x, w)
+
+
+def test_dispatch_bf16_full_size_grouped_properties():
+    """Full group-limited size: every copy equals its source row; sampled rows vs the oracle."""
+    d = W.make("grouped")
+    wl = d["wl"]
+    plan = plan_for(wl)
+    x = bf16_dev(d["x"])
+    plan.layout(dev(d["topk_idx"]))
+    recv, _, _ = plan.dispatch(x)
+    slot = plan.layout_out.slot_of
+    assert torch.equal(recv[slot.flatten().long()].view(torch.int16),
+                       x.repeat_interleave(wl.k, dim=0).view(torch.int16))
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(wl.T, 64, replace=False))
+    sl = slot.cpu().numpy()[sample]
+    o_recv, _ = oracle.dispatch_bf16(d["x"][sample], np.arange(64 * wl.k, dtype=np.int32).reshape(64, wl.k),
+                                     64 * wl.k)
+    np.testing.assert_array_equal(bits(recv[torch.from_numpy(sl.ravel()).long().cuda()]), o_recv)
+
+
+# --------------------------------------------------------------- fp8 dispatch
+
+def _dispatch_fp8_case(wl: W.Workload, idx, x):
+    plan = plan_for(wl)
+    plan.recv.view(torch.uint8).fill_(0x5A)
+    plan.recv_scales.fill_(-3.0)
+    plan.layout(dev(idx))
+    q, s, _ = plan.dispatch(bf16_dev(x))
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, idx)
+    oq, os_, _ = oracle.dispatch_fp8(x, L["slot_of"], wl.R)
+    live = np.zeros(wl.R, bool)
+    live[L["slot_of"][L["slot_of"] >= 0]] = True
+    gq = q.view(torch.uint8).cpu().numpy()
+    gs = s.cpu().numpy()
+    np.testing.assert_array_equal(gq[live], oq[live])
+    np.testing.assert_array_equal(gs[live].view(np.uint32), os_[live].view(np.uint32))
+    assert (gq[~live] == 0x5A).all() and (gs[~live] == -3.0).all()     # untouched rows
+    assert int(plan.layout_out.err_flags.item()) & ep.ERRF_TIMEOUT == 0
+
+
+@pytest.mark.parametrize("name,T", [("decode", None), ("skewed", 640), ("decode", 1), ("skewed", 33)])
+def test_dispatch_fp8_workloads(name, T):
+    wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)
+    d = W.make(wl)
+    _dispatch_fp8_case(wl, d["topk_idx"], d["x"])
+
+
+@pytest.mark.parametrize("T,H,E,k", [(1, 128, 4, 1), (9, 384, 8, 3), (70, 512, 16, 8), (5, 7168, 32, 8),
+                                     (300, 1024, 64, 4), (2, 65536, 4, 2), (160, 640, 8, 8)])
+def test_dispatch_fp8_shapes(T, H, E, k):
+    rng = np.random.default_rng(T * 3 + H)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < 0.1] = -1
+    scale = np.exp(rng.uniform(-20, 12, size=(T, H // 128, 1))).astype(np.float32)
+    xf = (rng.standard_normal((T, H // 128, 128)).astype(np.float32) * scale).reshape(T, H)
+    xf[:, :128] = 0.0                                        # an all-zero block per token
+    if H >= 384:
+        xf[:, 256:384] = np.float32(1e-30)                   # amax under the 1e-4 floor
+    x = W.to_bf16_bits(xf)
+    wl = W.Workload("s", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=True)
+    _dispatch_fp8_case(wl, idx, x)
+
+
+def test_dispatch_fp8_full_size_skewed_sampled():
+    d = W.make("skewed")
+    wl = d["wl"]
+    plan = plan_for(wl)
+    plan.layout(dev(d["topk_idx"]))
+    q, s, _ = plan.dispatch(bf16_dev(d["x"]))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    sample = np.sort(rng.choice(wl.T, 96, replace=False))
+    sl = plan.layout_out.slot_of.cpu().numpy()[sample].ravel()
+    n = len(sample)
+    oq, os_, _ = oracle.dispatch_fp8(d["x"][sample], np.arange(n * wl.k, dtype=np.int32).reshape(n, wl.k),
+                                     n * wl.k)
+    rows = torch.from_numpy(sl).long().cuda()
+    np.testing.assert_array_equal(q.view(torch.uint8)[rows].cpu().numpy(), oq)
+    np.testing.assert_array_equal(s[rows].cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
+# -------------------------------------------------------------------- combine
+
+def _combine_case(wl: W.Workload, idx, w, y_bits):
+    plan = plan_for(wl)
+    plan.layout(dev(idx))
+    out = plan.combine(bf16_dev(y_bits), dev(w))
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, idx)
+    assert_combine_close(bits(out), oracle.combine(y_bits, w, L["slot_of"]))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", None), ("skewed", 512),
+                                    ("grouped", 1024), ("tiny", 1)])
+def test_combine_workloads(name, T):
+    wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)
+    d = W.make(wl)
+    y = W.expert_rows(wl.R, wl.H)
+    _combine_case(wl, d["topk_idx"], d["topk_w"], y)
+
+
+def test_combine_random_scale_experts_tiny():
+    """y = bf16(s_e * x[src]) for each receive row (fake experts with a scale each)."""
+    d = W.make("tiny")
+    wl = d["wl"]
+    L = oracle_layout(wl, d["topk_idx"])
+    s_e = W.expert_scales(wl)
+    expert_of_row = np.repeat(np.arange(wl.E), L["counts"])
+    xf = oracle.bf16_to_f32(d["x"])
+    y = W.to_bf16_bits(xf[L["src_token"]] * s_e[expert_of_row][:, None])
+    _combine_case(wl, d["topk_idx"], d["topk_w"], y)
+
+
+@pytest.mark.parametrize("T,H,E,k,cap,mask", [(1, 8, 2, 1, None, 0.0), (3, 16, 4, 4, None, 0.5),
+                                              (129, 1032, 16, 5, None, 0.1), (40, 7168, 64, 8, 2, 0.0),
+                                              (7, 24, 32, 32, None, 0.2), (2, 65536, 8, 3, None, 0.0)])
+def test_combine_shapes(T, H, E, k, cap, mask):
+    rng = np.random.default_rng(T * 11 + H)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < mask] = -1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    wl = W.Workload("s", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=False,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    y = W.to_bf16_bits((rng.standard_normal((wl.R, H)) * 4).astype(np.float32))
+    _combine_case(wl, idx, w, y)
+
+
+def test_combine_full_size_grouped_sampled():
+    d = W.make("grouped")
+    wl = d["wl"]
+    y = W.expert_rows(wl.R, wl.H)
+    plan = plan_for(wl)
+    plan.layout(dev(d["topk_idx"]))
+    out = plan.combine(bf16_dev(y), dev(d["topk_w"]))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    sample = np.sort(rng.choice(wl.T, 256, replace=False))
+    sl = plan.layout_out.slot_of.cpu().numpy()[sample]
+    o = oracle.combine(y, d["topk_w"][sample], sl)
+    assert_combine_close(bits(out)[sample], o)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill", "grouped"])
+def test_round_trip_identity_experts_full_size(name):
+    """combine(dispatch(x)) with softmax weights returns x (sum of weights ~ 1)."""
+    d = W.make(name)
+    wl = d["wl"]
+    plan = plan_for(wl)
+    x = bf16_dev(d["x"])
+    plan.layout(dev(d["topk_idx"]))
+    recv, _, _ = plan.dispatch(x)
+    out = plan.combine(recv, dev(d["topk_w"])).float()
+    xf = x.float()
+    assert bool(((out - xf).abs() <= ATOL + RTOL * xf.abs()).all())
+
+
+def test_out_of_range_slots_are_skipped_and_flagged():
+    """slot_of entries outside [-1, R) never reach memory: skipped, EP_ERRF_BAD_SLOT set."""
+    T, H, E, k = 6, 256, 4, 2
+    rng = np.random.default_rng(9)
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    for fp8 in (False, True):
+        plan = ep.Plan(T, H, E, k, fp8=fp8)
+        slot = np.arange(T * k, dtype=np.int32).reshape(T, k)
+        slot[1, 0] = plan.R + 5
+        slot[4, 1] = -3
+        sentinel = 0x11
+        plan.recv.view(torch.uint8).fill_(sentinel)
+        plan.layout_out.err_flags.zero_()
+        recv, _, _ = plan.dispatch(bf16_dev(x), slot_of=dev(slot))
+        torch.cuda.synchronize()
+        assert int(plan.layout_out.err_flags.item()) == ep.ERRF_BAD_SLOT
+        raw = recv.view(torch.uint8).cpu().numpy()
+        assert (raw[2 * 1 + 0] == sentinel).all() and (raw[4 * 2 + 1] == sentinel).all()
+        assert not (raw[0] == sentinel).all()
+    plan = ep.Plan(T, H, E, k)
+    plan.layout_out.err_flags.zero_()
+    y = W.to_bf16_bits(rng.standard_normal((plan.R, H)).astype(np.float32))
+    w = np.ones((T, k), np.float32)
+    out = plan.combine(bf16_dev(y), dev(w), slot_of=dev(slot))
+    torch.cuda.synchronize()
+    assert int(plan.layout_out.err_flags.item()) == ep.ERRF_BAD_SLOT
+    o = oracle.combine(y, w, np.where((slot >= 0) & (slot < plan.R), slot, -1).astype(np.int32))
+    assert_combine_close(bits(out), o)
