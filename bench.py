@@ -10,10 +10,13 @@ Metric: effective HBM GB/s of the step = algorithmic bytes (what the method
 must move; see algorithmic_bytes) / device time, plus per-kernel us/call, GB/s
 and fraction of the measured HBM copy bandwidth.
 
-Timing: inputs resident in HBM; the L2 (129 MB) is flushed by writing a
-512 MB buffer before every timed step; each step is one CUDA-graph replay of
-the three calls, bracketed by CUDA events on the launching stream.  Kernels
-are also timed one at a time the same way.  e2e: the same step through the
+Timing: inputs resident in HBM; the L2 (129 MB) is flushed before every timed
+step by writing a 512 MB buffer and then reading another 512 MB (so it holds
+only clean, unrelated lines); each step is one CUDA-graph replay of the three
+calls, bracketed by CUDA events on the launching stream.  Per-kernel times
+come from a second graph of the same step with event-record nodes between the
+kernels (one graph per kernel where torch lacks such events).  e2e: the same
+step through the
 public API with pinned host inputs, host->device copies and the device->host
 read of the combined output inside the timed region.
 
@@ -234,6 +237,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
     y_d = torch.randn((plan.R, wl.H), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_src = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush_dst = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def flush_l2():
+        # Write a buffer 4x the L2, then read another one: the L2 ends up
+        # holding only clean lines of unrelated data, so the timed kernels
+        # neither hit their own data nor pay for earlier dirty lines.
+        flush.zero_()
+        torch.sum(flush_src, dim=0, keepdim=True, out=flush_dst)
     n_live = int((inp["topk_idx"] >= 0).sum())
     nbytes = algorithmic_bytes(wl, n_live)
     step_bytes = sum(nbytes.values())
@@ -269,18 +281,50 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             fn()
         return g
 
-    graphs = {"step": capture(do_step), "layout": capture(do_layout), "dispatch": capture(do_dispatch),
-              "combine": capture(do_combine)}
+    # Event-record nodes between the kernels of a second step graph time each
+    # kernel inside the step; torch without such events falls back to one
+    # graph per kernel (launch latency included).
+    try:
+        inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    except TypeError:
+        inner = None
+
+    def do_step_marked():
+        inner[0].record()
+        do_layout()
+        inner[1].record()
+        do_dispatch()
+        inner[2].record()
+        do_combine()
+        inner[3].record()
+
+    graphs = {"step": capture(do_step)}
+    if inner is not None:
+        graphs["marked"] = capture(do_step_marked)
+    else:
+        graphs.update(layout=capture(do_layout), dispatch=capture(do_dispatch), combine=capture(do_combine))
     stream = torch.cuda.current_stream()
 
     def timed(g, n):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for a, b in evs:
-            flush.zero_()
+            flush_l2()
             a.record(stream)
             g.replay()
             b.record(stream)
         return evs
+
+    if args.profile:
+        # Only the step kernels (for ncu launch lists): W + K flushed graph replays.
+        timed(graphs["step"], args.warmup + args.steps)
+        torch.cuda.synchronize()
+        flags = int(plan.layout_out.err_flags.item())
+        if rank == 0:
+            print(json.dumps({"profile_run": wl.name, "steps": args.warmup + args.steps,
+                              "launches_per_step": launches_per_step, "err_flags": flags}))
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -305,15 +349,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     wall = time.perf_counter() - t0
     step_ms = [a.elapsed_time(b) for a, b in step_evs]
 
-    # ---- per-kernel times, same flush discipline
-    reps = max(args.steps, 20)
-    per_kernel = {}
-    for name in ("layout", "dispatch", "combine"):
-        evs = timed(graphs[name], reps)
-        torch.cuda.synchronize()
-        ms = [a.elapsed_time(b) for a, b in evs]
-        per_kernel[name] = dict(us=round(statistics.median(ms) * 1e3, 3),
-                                us_mean=round(statistics.fmean(ms) * 1e3, 3))
+    # ---- per-kernel times, same flush discipline, K more steps
+    names = ("layout", "dispatch", "combine")
+    kernel_ms = {n: [] for n in names}
+    if inner is not None:
+        for _ in range(args.steps):
+            timed(graphs["marked"], 1)
+            torch.cuda.synchronize()
+            for q, n in enumerate(names):
+                kernel_ms[n].append(inner[q].elapsed_time(inner[q + 1]))
+    else:
+        for n in names:
+            evs = timed(graphs[n], args.steps)
+            torch.cuda.synchronize()
+            kernel_ms[n] = [a.elapsed_time(b) for a, b in evs]
+    per_kernel = {n: dict(us=round(statistics.median(kernel_ms[n]) * 1e3, 3),
+                          us_mean=round(statistics.fmean(kernel_ms[n]) * 1e3, 3),
+                          timed="inside the step graph" if inner is not None else "own graph, launch included")
+                  for n in names}
 
     # ---- e2e through the public API with host buffers
     x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -324,7 +377,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     d2h = out_h.numel() * 2
     e2e_ms = []
     for it in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         x_d.copy_(x_h, non_blocking=True)
@@ -371,7 +424,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
                    "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
                    "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
-                   "step_bytes": step_bytes, "l2": "flushed (512 MB write) before every timed step",
+                   "step_bytes": step_bytes, "l2": "flushed before every timed step (512 MB write, then 512 MB read: cold, clean L2)",
                    "timing": "CUDA-graph replay of layout+dispatch+combine, CUDA events per step",
                    "parallelism": f"replicas x{world}"},
         "kernels": per_kernel,
@@ -429,6 +482,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=tuple(W.WORKLOADS), default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="run only W+K flushed step replays (for an ncu launch list); prints no bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

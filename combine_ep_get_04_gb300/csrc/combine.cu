@@ -5,10 +5,15 @@
 // Combine is the reverse of dispatch and is measured beside it in "Pipeline
 // direct NVLink dispatch with triple-buffered prefetch" (DeepEP PR #693),
 // Validation table.  It reads k rows per token and writes one, so it is a
-// gather bound by HBM reads: each thread owns 16 bytes (8 channels) of one
-// token, issues the k independent 16-byte row loads before it does any
-// arithmetic, and stores one 16-byte vector.  No tensor cores: there is no
-// contraction, only k multiply-adds per output element.
+// gather bound by HBM reads.  The gather is done by the TMA engine: for a
+// unit (token t, slice of its row) a producer warp issues one bulk copy per
+// valid slot, y[slot_of[t,j]] slice -> shared stage row j, completing on the
+// stage's "full" mbarrier.  A ring of NS stages keeps up to NS units in flight
+// per CTA -- far more bytes than registers could hold -- while consumer warps
+// sum the k staged rows in fp32 (16 bytes per thread per step), store the
+// bf16 result with 16-byte coalesced stores and hand the stage back through
+// its "empty" mbarrier.  No tensor cores: there is no contraction, only k
+// multiply-adds per output element.
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
@@ -16,28 +21,26 @@ namespace ep {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBatch = 8;   // rows loaded before they are summed
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kStages = 4;
+constexpr uint32_t kStageBytesMax = 16384;   // k rows x slice bytes per stage
 
 struct Args {
-    const uint4* y;
+    const unsigned char* y;
     const float* topk_w;
     const int32_t* slot_of;
-    uint4* out;
+    unsigned char* out;
     uint32_t* err_flags;
-    int64_t R;       // rows of y
-    int64_t total;   // T * H8
-    int H8;          // H / 8
+    int64_t R;               // rows of y
+    int64_t units;           // T * slices
+    int64_t row_bytes;       // H * 2
+    int slices;              // units per token row
     int k;
+    uint32_t slice_bytes;    // multiple of 16
+    uint32_t stage_bytes;    // k * slice_bytes (rows of one stage are slice_bytes apart)
 };
-
-__device__ __forceinline__ uint4 load_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
@@ -48,67 +51,178 @@ __device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4
     }
 }
 
+// Warp 0 produces (indices, weights, bulk copies into a ring of NS stages);
+// warps 1..kConsumerWarps consume (sum, convert, store) and hand each stage
+// back through its "empty" mbarrier, so index loads and copies of later units
+// overlap the arithmetic of earlier ones.
+template <int NS>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
-    const int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (g >= a.total) return;
-    const int64_t t = g / a.H8;
-    const int c = (int)(g - t * a.H8);
-    const int32_t* so = a.slot_of + t * a.k;
-    const float* wt = a.topk_w + t * a.k;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);                     // [NS] data landed
+    uint64_t* empty = full + NS;                                            // [NS] stage free again
+    float* w_s = reinterpret_cast<float*>(smem + 128);                      // [NS][32] weights, 0 if no row
+    uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + 128 + NS * 128);  // [NS] valid-row bits
+    unsigned char* stages = smem + 256 + NS * 128;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t first = blockIdx.x;
+    if (first >= a.units) return;
+    const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
 
-    float acc[8];
+    if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-
-    for (int j0 = 0; j0 < a.k; j0 += kBatch) {
-        int32_t s[kBatch];
-        float w[kBatch];
-        uint4 v[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            s[u] = (j0 + u < a.k) ? __ldg(so + j0 + u) : -1;
-            if (s[u] < -1 || s[u] >= a.R) {
-                if (c == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
-                s[u] = -1;
-            }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (s[u] >= 0) {
-                w[u] = __ldg(wt + j0 + u);
-                v[u] = load_stream(a.y + (int64_t)s[u] * a.H8 + c);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (s[u] >= 0) accumulate(acc, w[u], v[u]);
-        }
+        fence_mbar_init();
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    a.out[g] = o;
+    __syncthreads();
+
+    bool ok = true;
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        // The slot and weight of unit i+1 are loaded while unit i is issued.
+        auto load_index = [&](int64_t i, int32_t& slot, float& w) {
+            const int64_t t = (first + i * gridDim.x) / a.slices;
+            slot = -1;
+            w = 0.f;
+            if (lane < a.k) {
+                slot = __ldg(a.slot_of + t * a.k + lane);
+                w = __ldg(a.topk_w + t * a.k + lane);
+            }
+        };
+        int32_t next_slot;
+        float next_w;
+        load_index(0, next_slot, next_w);
+        int64_t i = 0;
+        for (; i < n_mine; ++i) {
+            const int64_t u = first + i * gridDim.x;
+            const int64_t t = u / a.slices;
+            const int sl = (int)(u - t * a.slices);
+            const int s = (int)(i % NS);
+            int32_t slot = next_slot;
+            float w = next_w;
+            if (i + 1 < n_mine) load_index(i + 1, next_slot, next_w);
+            if (slot < -1 || slot >= a.R) {
+                if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
+                slot = -1;
+            }
+            if (slot < 0) w = 0.f;
+            const uint32_t valid = __ballot_sync(kFull, slot >= 0);
+            if (i >= NS) {   // wait until the consumers released this stage's previous unit
+                ok = __all_sync(kFull, mbar_wait(&empty[s], (uint32_t)(((i / NS) - 1) & 1)));
+                if (!ok) break;
+            }
+            if (lane < a.k) w_s[s * 32 + lane] = w;
+            if (lane == 0) mask_s[s] = valid;
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(valid) * a.slice_bytes);
+            __syncwarp();
+            if (slot >= 0) {
+                bulk_load(stages + (size_t)s * a.stage_bytes + (size_t)lane * a.slice_bytes,
+                          a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes,
+                          &full[s]);
+            }
+        }
+        if (!ok) {
+            // Copies already issued target this CTA's shared memory: let them
+            // land (each wait bounded) before the CTA exits.
+            if (lane == 0) {
+                for (int64_t r = (i > NS ? i - NS : 0); r < i; ++r) {
+                    (void)mbar_wait(&full[r % NS], (uint32_t)((r / NS) & 1));
+                }
+                if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ctid = tid - 32;
+    const int chunks = (int)(a.slice_bytes / 16);
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int64_t u = first + i * gridDim.x;
+        const int64_t t = u / a.slices;
+        const int sl = (int)(u - t * a.slices);
+        const int s = (int)(i % NS);
+        ok = __all_sync(kFull, mbar_wait(&full[s], (uint32_t)((i / NS) & 1)));
+        if (!ok) break;
+        const uint32_t valid = mask_s[s];
+        const unsigned char* st = stages + (size_t)s * a.stage_bytes;
+        unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
+        for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            for (int j = 0; j < a.k; ++j) {
+                if (valid & (1u << j)) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
+                    accumulate(acc, w_s[s * 32 + j], v);
+                }
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(dst + ch * 16) = o;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!ok && lane == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+}
+
+// Number of slices a row of n granules is cut into: the smallest divisor d of
+// n whose slices hold at most max_per granules and give T*d >= want units;
+// slices never drop below min_per granules once one size fits.
+int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t want) {
+    int best = 0;
+    for (int64_t d = 1; d <= n; ++d) {
+        if (n % d) continue;
+        const int64_t per = n / d;
+        if (per > max_per) continue;
+        if (best && per < min_per) break;
+        best = (int)d;
+        if (T * d >= want) break;
+    }
+    return best ? best : (int)n;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t stream) {
-    (void)num_sms;
     if (p.T == 0) return cudaSuccess;
     Args a{};
-    a.y = static_cast<const uint4*>(p.y);
+    a.y = static_cast<const unsigned char*>(p.y);
     a.topk_w = p.topk_w;
     a.slot_of = p.slot_of;
-    a.out = static_cast<uint4*>(p.out);
+    a.out = static_cast<unsigned char*>(p.out);
     a.err_flags = p.err_flags;
     a.R = p.R;
-    a.H8 = p.H / 8;
     a.k = p.k;
-    a.total = (int64_t)p.T * a.H8;
-    const int64_t grid = (a.total + kThreads - 1) / kThreads;
-    combine_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(a);
+    a.row_bytes = (int64_t)p.H * 2;
+    // A stage holds k slices; slices of at most kStageBytesMax / k bytes, at
+    // least 256 bytes once one size fits, enough units for ~4 per SM.
+    const int64_t vec16 = a.row_bytes / 16;
+    const int64_t max_per = (int64_t)(kStageBytesMax / 16) / p.k;
+    a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, 4LL * num_sms);
+    a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+    a.stage_bytes = a.slice_bytes * (uint32_t)p.k;
+    a.units = (int64_t)p.T * a.slices;
+    const size_t smem = 256 + (size_t)kStages * 128 + (size_t)kStages * a.stage_bytes;
+    auto kern = combine_kernel<kStages>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms * per_sm;
+    if (grid > a.units) grid = a.units;
+    kern<<<(unsigned)grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -71,6 +71,21 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
         for (int64_t i = 0; i < LA && i < n_mine; ++i) issue_load(i);
     }
 
+    // Lane j holds the slot (and weight) of copy j of the next unit, loaded
+    // one unit ahead.
+    auto load_index = [&](int64_t i, int32_t& slot, float& w) {
+        const int64_t t = (first + i * gridDim.x) / a.slices;
+        slot = -1;
+        w = 0.f;
+        if (lane < a.k) {
+            slot = __ldg(a.slot_of + t * a.k + lane);
+            if (a.recv_w != nullptr) w = __ldg(a.topk_w + t * a.k + lane);
+        }
+    };
+    int32_t next_slot;
+    float next_w;
+    load_index(0, next_slot, next_w);
+
     bool ok = true;
     int64_t i = 0;
     for (; i < n_mine; ++i) {
@@ -85,15 +100,12 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
             __syncwarp();
             if (lane == 0) issue_load(i + LA);
         }
-        int32_t slot = -1;
-        float w = 0.f;
-        if (lane < a.k) {
-            slot = __ldg(a.slot_of + t * a.k + lane);
-            if (slot < -1 || slot >= a.R) {
-                if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
-                slot = -1;
-            }
-            if (a.recv_w != nullptr && sl == 0 && slot >= 0) w = __ldg(a.topk_w + t * a.k + lane);
+        int32_t slot = next_slot;
+        const float w = next_w;
+        if (i + 1 < n_mine) load_index(i + 1, next_slot, next_w);
+        if (slot < -1 || slot >= a.R) {
+            if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
+            slot = -1;
         }
         ok = __all_sync(kFull, mbar_wait(&bars[s], (uint32_t)((i / NS) & 1)));
         if (!ok) break;
