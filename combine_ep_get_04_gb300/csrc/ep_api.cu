@@ -75,6 +75,10 @@ ep_status_t launched(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace ep {
+void record_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace ep
+
 extern "C" {
 
 int32_t ep_abi_version(void) { return 100; }

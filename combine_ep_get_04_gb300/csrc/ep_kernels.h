@@ -9,6 +9,9 @@
 
 namespace ep {
 
+// Sets the text ep_last_error() returns on the calling thread.
+void record_last_error(const char* msg);
+
 // ----------------------------------------------------------------- layout
 
 constexpr int64_t kLayoutChunk = 1024;   // entries ranked by one CTA

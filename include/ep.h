@@ -140,6 +140,32 @@ EP_API ep_status_t ep_get_layout(const ep_shape_t *shape, const int32_t *topk_id
                           uint32_t *err_flags, ep_stream_t stream);
 
 /*
+ * ep_get_layout_static -- ep_get_layout without a caller-supplied workspace.
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot allocate device memory where they compute the layout (code
+ * confined to a fixed memory budget owned by a host framework, or a latency-
+ * critical path on which a device allocation could stall the device).
+ *
+ * Same arguments, outputs, ordering and err_flags as ep_get_layout, minus
+ * workspace / workspace_bytes.  Scratch comes from a 1 MiB array built into
+ * the library (every GPU that loads the library holds it until the process
+ * exits): shapes needing more than 1 MiB of layout workspace, i.e.
+ * ceil(T*k / 1024) * E * 4 bytes > 1 MiB (about 2^20 routing entries at
+ * E = 256), return EP_ERR_UNSUPPORTED; smaller shapes that need no workspace
+ * use none.  The array's device address is looked up on the first call that
+ * needs it on each device, with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (each call writes every entry it reads, so nothing
+ * needs clearing); calls whose work overlaps on the GPU race on it and must
+ * be ordered by the caller.  Allocates nothing.
+ */
+EP_API ep_status_t ep_get_layout_static(const ep_shape_t *shape, const int32_t *topk_idx,
+                          int32_t *counts, int32_t *offsets,
+                          int32_t *part_counts, int32_t *part_offsets,
+                          int32_t *slot_of, int32_t *src_token, int32_t *src_k,
+                          uint32_t *err_flags, ep_stream_t stream);
+
+/*
  * ep_dispatch -- copy every token's hidden row to each receive row it is
  * routed to (slot_of from ep_get_layout; R = ep_recv_rows(shape)).
  *
