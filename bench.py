@@ -215,6 +215,22 @@ def time_oracle(wl: W.Workload, budget_s: float = 12.0, min_reps: int = 3) -> di
                 seconds=round(sum(times), 2), host_cpus=os.cpu_count())
 
 
+# ------------------------------------------------------------- replicas
+
+def max_over_ranks(vals: list[float], dist=None, device: str = "cpu") -> list[float]:
+    """Element-wise max of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(step_bytes: int, world: int, ms: float) -> float:
+    """Whole-job GB/s of N replicas that each moved step_bytes in ms (max over ranks)."""
+    return world * step_bytes / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------- GPU
 
 def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
@@ -398,10 +414,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     ms_mean = statistics.fmean(step_ms)
     e2e_mean = statistics.fmean(e2e_ms)
-    vals = torch.tensor([ms_mean, e2e_mean, wall], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_mean, e2e_mean, wall = vals.tolist()
+    ms_mean, e2e_mean, wall = max_over_ranks([ms_mean, e2e_mean, wall], dist, "cuda")
     if dist is not None:
         dist.destroy_process_group()
     if rank != 0:
@@ -415,8 +428,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     dk = per_kernel[dominant]
     ach = nbytes[dominant] / (dk["us_mean"] * 1e-6) / 1e9
     traffic = ncu_traffic(wl.name, dominant)
-    value = world * step_bytes / (ms_mean * 1e-3) / 1e9
-    e2e_value = world * step_bytes / (e2e_mean * 1e-3) / 1e9
+    value = replica_throughput(step_bytes, world, ms_mean)
+    e2e_value = replica_throughput(step_bytes, world, e2e_mean)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_mean, 5), "higher_is_better": True, "scaling": "weak",
