@@ -263,10 +263,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         flush.zero_()
         torch.sum(flush_src, dim=0, keepdim=True, out=flush_dst)
     n_live = int((inp["topk_idx"] >= 0).sum())
-    nbytes = algorithmic_bytes(wl, n_live)
-    step_bytes = sum(nbytes.values())
+    kbytes = algorithmic_bytes(wl, n_live)
+    step_bytes = sum(kbytes.values())
     layout_launches = 2 if plan.workspace_bytes > 0 else 1
-    launches_per_step = layout_launches + 2
 
     def do_layout():
         plan.layout(idx_d, clear_flags=False)
@@ -274,13 +273,29 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     def do_dispatch():
         plan.dispatch(x_d)
 
+    def do_layout_dispatch():
+        plan.layout_dispatch(idx_d, x_d, clear_flags=False)
+
     def do_combine():
         plan.combine(y_d, w_d)
 
+    # The step: ep_layout_dispatch (one launch for small batches) + ep_combine;
+    # larger batches run the three calls that ep_layout_dispatch would make.
+    fused = ep.fused_layout_dispatch(wl.T, wl.k, wl.E)
+    if fused:
+        stages = [("layout_dispatch", do_layout_dispatch, kbytes["layout"] + kbytes["dispatch"], 1),
+                  ("combine", do_combine, kbytes["combine"], 1)]
+    else:
+        stages = [("layout", do_layout, kbytes["layout"], layout_launches),
+                  ("dispatch", do_dispatch, kbytes["dispatch"], 1),
+                  ("combine", do_combine, kbytes["combine"], 1)]
+    names = tuple(n for n, _, _, _ in stages)
+    nbytes = {n: b for n, _, b, _ in stages}
+    launches_per_step = sum(c for _, _, _, c in stages)
+
     def do_step():
-        do_layout()
-        do_dispatch()
-        do_combine()
+        for _, fn, _, _ in stages:
+            fn()
 
     plan.layout_out.err_flags.zero_()
     side = torch.cuda.Stream()
@@ -301,24 +316,21 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # kernel inside the step; torch without such events falls back to one
     # graph per kernel (launch latency included).
     try:
-        inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stages) + 1)]
     except TypeError:
         inner = None
 
     def do_step_marked():
-        inner[0].record()
-        do_layout()
-        inner[1].record()
-        do_dispatch()
-        inner[2].record()
-        do_combine()
-        inner[3].record()
+        for q, (_, fn, _, _) in enumerate(stages):
+            inner[q].record()
+            fn()
+        inner[len(stages)].record()
 
     graphs = {"step": capture(do_step)}
     if inner is not None:
         graphs["marked"] = capture(do_step_marked)
     else:
-        graphs.update(layout=capture(do_layout), dispatch=capture(do_dispatch), combine=capture(do_combine))
+        graphs.update({n: capture(fn) for n, fn, _, _ in stages})
     stream = torch.cuda.current_stream()
 
     def timed(g, n):
@@ -366,7 +378,6 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     step_ms = [a.elapsed_time(b) for a, b in step_evs]
 
     # ---- per-kernel times, same flush discipline, K more steps
-    names = ("layout", "dispatch", "combine")
     kernel_ms = {n: [] for n in names}
     if inner is not None:
         for _ in range(args.steps):
@@ -424,7 +435,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     for name, r in per_kernel.items():
         gbs = nbytes[name] / (r["us"] * 1e-6) / 1e9
         r.update(bytes=nbytes[name], gbs=round(gbs, 1), frac_of_hbm=round(gbs / peak, 4))
-    dominant = max(("dispatch", "combine", "layout"), key=lambda n: per_kernel[n]["us"])
+    dominant = max(names, key=lambda n: per_kernel[n]["us"])
     dk = per_kernel[dominant]
     ach = nbytes[dominant] / (dk["us_mean"] * 1e-6) / 1e9
     traffic = ncu_traffic(wl.name, dominant)
@@ -438,7 +449,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
                    "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
                    "step_bytes": step_bytes, "l2": "flushed before every timed step (512 MB write, then 512 MB read: cold, clean L2)",
-                   "timing": "CUDA-graph replay of layout+dispatch+combine, CUDA events per step",
+                   "timing": "CUDA-graph replay of the step, CUDA events per step",
+                   "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine",
                    "parallelism": f"replicas x{world}"},
         "kernels": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,

@@ -28,7 +28,18 @@ from ._lib import (CAPACITY, ERRF_BAD_EXPERT, ERRF_BAD_SLOT, ERRF_CAPACITY, ERRF
 __all__ = ["Plan", "Layout", "Shape", "EPError", "get_layout", "dispatch", "combine", "load", "library_path",
            "PACKED", "CAPACITY", "PAYLOAD_BF16", "PAYLOAD_FP8_E4M3", "ERRF_BAD_EXPERT", "ERRF_CAPACITY",
            "ERRF_TIMEOUT", "ERRF_BAD_SLOT", "MAX_EXPERTS", "MAX_TOPK", "EXPORTED", "make_shape", "recv_rows",
-           "layout_workspace_bytes"]
+           "layout_workspace_bytes", "fused_layout_dispatch", "FUSED_MAX_N", "FUSED_MAX_T"]
+
+
+# Batches the library dispatches with the layout folded into one launch
+# (same limits as the C library's fused path).
+FUSED_MAX_N = 2048
+FUSED_MAX_T = 2048
+
+
+def fused_layout_dispatch(T: int, k: int, E: int) -> bool:
+    """True when ep_layout_dispatch runs as a single kernel for this shape."""
+    return 1 <= T <= FUSED_MAX_T and T * k <= FUSED_MAX_N and E <= MAX_EXPERTS
 
 
 def make_shape(T: int, H: int, E: int, k: int, num_partitions: int = 1, capacity: int | None = None) -> Shape:
@@ -147,6 +158,31 @@ class Plan:
             _ptr(self.recv_w) if topk_w is not None else None, _ptr(self.layout_out.err_flags), _stream(stream))
         check(st, "ep_dispatch")
         return self.recv, self.recv_scales, self.recv_w
+
+    def layout_dispatch(self, topk_idx: torch.Tensor, x: torch.Tensor, topk_w: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None, clear_flags: bool = True):
+        """layout() then dispatch() in one call (one launch for small batches).
+
+        Returns (layout, recv, recv_scales, recv_w)."""
+        s = self.shape
+        L = self.layout_out
+        if clear_flags:
+            L.err_flags.zero_()
+        if tuple(topk_idx.shape) != (s.T, s.k):
+            raise ValueError(f"topk_idx must be [{s.T}, {s.k}], got {tuple(topk_idx.shape)}")
+        if tuple(x.shape) != (s.T, s.H):
+            raise ValueError(f"x must be [{s.T}, {s.H}], got {tuple(x.shape)}")
+        if self.recv_w is not None and topk_w is None:
+            raise ValueError("this plan routes weights: pass topk_w")
+        st = load().ep_layout_dispatch(
+            ctypes.byref(s), _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(x, torch.bfloat16, "x"),
+            _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), PAYLOAD_FP8_E4M3 if self.fp8 else PAYLOAD_BF16,
+            _ptr(L.counts), _ptr(L.offsets), _ptr(L.part_counts), _ptr(L.part_offsets), _ptr(L.slot_of),
+            _ptr(L.src_token), _ptr(L.src_k), _ptr(self.recv), _ptr(self.recv_scales),
+            _ptr(self.recv_w) if topk_w is not None else None, _ptr(self.workspace), self.workspace_bytes,
+            _ptr(L.err_flags), _stream(stream))
+        check(st, "ep_layout_dispatch")
+        return L, self.recv, self.recv_scales, self.recv_w
 
     def combine(self, y: torch.Tensor, topk_w: torch.Tensor, stream: torch.cuda.Stream | None = None,
                 out: torch.Tensor | None = None, slot_of: torch.Tensor | None = None) -> torch.Tensor:

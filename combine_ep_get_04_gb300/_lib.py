@@ -30,7 +30,8 @@ EP_ERR_CUDA = 3
 
 # Every symbol include/ep.h declares.
 EXPORTED = ("ep_recv_rows", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_static",
-            "ep_dispatch", "ep_combine", "ep_status_string", "ep_last_error", "ep_abi_version")
+            "ep_dispatch", "ep_layout_dispatch", "ep_combine", "ep_status_string", "ep_last_error",
+            "ep_abi_version")
 
 
 class Shape(ctypes.Structure):
@@ -77,6 +78,9 @@ def load() -> ctypes.CDLL:
     lib.ep_get_layout_static.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_dispatch.restype = ctypes.c_int
     lib.ep_dispatch.argtypes = [sp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.ep_layout_dispatch.restype = ctypes.c_int
+    lib.ep_layout_dispatch.argtypes = [sp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       ctypes.c_size_t, vp, vp]
     lib.ep_combine.restype = ctypes.c_int
     lib.ep_combine.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.ep_status_string.restype = ctypes.c_char_p

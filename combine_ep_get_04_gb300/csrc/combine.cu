@@ -212,17 +212,30 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
     a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
     a.stage_bytes = a.slice_bytes * (uint32_t)p.k;
     a.units = (int64_t)p.T * a.slices;
-    const size_t smem = 256 + (size_t)kStages * 128 + (size_t)kStages * a.stage_bytes;
-    auto kern = combine_kernel<kStages>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // If one single-stage CTA per unit fits on the GPU at once (small
+    // batches), launch exactly that: every unit starts immediately.  Otherwise
+    // a persistent grid of kStages-deep rings.
+    auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
+        smem = 256 + (size_t)ns * 128 + (size_t)ns * a.stage_bytes;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
+        return e;
+    };
+    size_t smem = 0;
+    int64_t ctas = 0;
+    cudaError_t err = resident(combine_kernel<1>, 1, smem, ctas);
     if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (a.units <= ctas) {
+        combine_kernel<1><<<(unsigned)a.units, kThreads, smem, stream>>>(a);
+        return cudaGetLastError();
+    }
+    err = resident(combine_kernel<kStages>, kStages, smem, ctas);
     if (err != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)num_sms * per_sm;
-    if (grid > a.units) grid = a.units;
-    kern<<<(unsigned)grid, kThreads, smem, stream>>>(a);
+    const int64_t grid = ctas < a.units ? ctas : a.units;
+    combine_kernel<kStages><<<(unsigned)grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -186,6 +186,66 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const void* x, const float* top
                     "dispatch launch");
 }
 
+ep_status_t ep_layout_dispatch(const ep_shape_t* shape, const int32_t* topk_idx, const void* x,
+                               const float* topk_w, int32_t payload, int32_t* counts, int32_t* offsets,
+                               int32_t* part_counts, int32_t* part_offsets, int32_t* slot_of, int32_t* src_token,
+                               int32_t* src_k, void* recv, float* recv_scales, float* recv_w, void* workspace,
+                               size_t workspace_bytes, uint32_t* err_flags, ep_stream_t stream) {
+    ep_status_t st = check_shape(shape);
+    if (st != EP_OK) return st;
+    const int64_t N = (int64_t)shape->T * shape->k;
+    if (!ep::fused_layout_dispatch_fits(N, shape->T, shape->E) || shape->T == 0) {
+        st = ep_get_layout(shape, topk_idx, counts, offsets, part_counts, part_offsets, slot_of, src_token, src_k,
+                           workspace, workspace_bytes, err_flags, stream);
+        if (st != EP_OK) return st;
+        return ep_dispatch(shape, x, topk_w, slot_of, payload, recv, recv_scales, recv_w, err_flags, stream);
+    }
+    // The same checks as ep_get_layout and ep_dispatch, before anything is launched.
+    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3)
+        return fail(EP_ERR_INVALID_ARG, "payload = %d is not a payload format", payload);
+    const bool fp8 = payload == EP_PAYLOAD_FP8_E4M3;
+    if (fp8 && shape->H % 128 != 0) return fail(EP_ERR_INVALID_ARG, "fp8 payload needs H %% 128 == 0 (H = %d)", shape->H);
+    if (topk_idx == nullptr || slot_of == nullptr || x == nullptr || recv == nullptr)
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / slot_of / x / recv is NULL");
+    if (counts == nullptr || offsets == nullptr || part_counts == nullptr || part_offsets == nullptr ||
+        src_token == nullptr || src_k == nullptr)
+        return fail(EP_ERR_INVALID_ARG, "counts / offsets / part_counts / part_offsets / src_token / src_k is NULL");
+    if (!aligned16(x) || !aligned16(recv)) return fail(EP_ERR_INVALID_ARG, "x and recv must be 16-byte aligned");
+    if (fp8 && (recv_scales == nullptr || !aligned16(recv_scales)))
+        return fail(EP_ERR_INVALID_ARG, "fp8 payload needs 16-byte aligned recv_scales");
+    if (recv_w != nullptr && topk_w == nullptr) return fail(EP_ERR_INVALID_ARG, "recv_w needs topk_w");
+    int num_sms = 0;
+    st = device_info(&num_sms);
+    if (st != EP_OK) return st;
+
+    ep::FusedLaunch f{};
+    f.topk_idx = topk_idx;
+    f.x = x;
+    f.topk_w = topk_w;
+    f.counts = counts;
+    f.offsets = offsets;
+    f.part_counts = part_counts;
+    f.part_offsets = part_offsets;
+    f.slot_of = slot_of;
+    f.src_token = src_token;
+    f.src_k = src_k;
+    f.recv = recv;
+    f.recv_scales = recv_scales;
+    f.recv_w = recv_w;
+    f.err_flags = err_flags;
+    f.R = rows_of(shape);
+    f.T = shape->T;
+    f.H = shape->H;
+    f.E = shape->E;
+    f.k = shape->k;
+    f.P = shape->num_partitions;
+    f.mode = shape->mode;
+    f.cap = shape->capacity;
+    f.fp8 = fp8 ? 1 : 0;
+    return launched(ep::launch_layout_dispatch(f, num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                    "layout+dispatch launch");
+}
+
 ep_status_t ep_combine(const ep_shape_t* shape, const void* y, const float* topk_w, const int32_t* slot_of,
                        void* out, uint32_t* err_flags, ep_stream_t stream) {
     ep_status_t st = check_shape(shape);

@@ -58,6 +58,33 @@ struct DispatchParams {
 cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream_t stream);
 
+// ------------------------------------------------ layout + dispatch fused
+
+constexpr int64_t kFusedMaxN = 2048;   // routing entries: every CTA counts them all
+constexpr int64_t kFusedMaxT = 2048;
+
+struct FusedLaunch {
+    const int32_t* topk_idx;
+    const void* x;
+    const float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* part_counts;
+    int32_t* part_offsets;
+    int32_t* slot_of;
+    int32_t* src_token;
+    int32_t* src_k;
+    void* recv;
+    float* recv_scales;
+    float* recv_w;
+    uint32_t* err_flags;
+    int64_t R;
+    int T, H, E, k, P, mode, cap, fp8;
+};
+
+bool fused_layout_dispatch_fits(int64_t N, int64_t T, int E);
+cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream_t stream);
+
 // ---------------------------------------------------------------- combine
 
 struct CombineParams {

@@ -194,6 +194,31 @@ EP_API ep_status_t ep_dispatch(const ep_shape_t *shape, const void *x,
                         float *recv_w, uint32_t *err_flags, ep_stream_t stream);
 
 /*
+ * ep_layout_dispatch -- ep_get_layout followed by ep_dispatch, in one launch
+ * when the batch is small (T*k <= 2048 and T <= 2048), otherwise as those two
+ * calls.  Small decode batches are where a launch matters ("Why does DeepEP
+ * LL kernel use double send/recv/signal buffers?", last answer: the design
+ * targets high tokens per second), and the v1 low-latency path avoided a
+ * separate count exchange ("Why did DeepEP v2 drop the double-buffer
+ * design...", question).
+ *
+ * Arguments, outputs, ordering, checks and err_flags are exactly those of
+ * ep_get_layout (topk_idx .. src_k, workspace, workspace_bytes) and
+ * ep_dispatch (x, topk_w, payload, recv, recv_scales, recv_w) on the same
+ * shape; every output is bit-identical to the two separate calls.  The
+ * workspace is only used on the two-call path (size from
+ * ep_layout_workspace_bytes).
+ */
+EP_API ep_status_t ep_layout_dispatch(const ep_shape_t *shape, const int32_t *topk_idx,
+                          const void *x, const float *topk_w, int32_t payload,
+                          int32_t *counts, int32_t *offsets,
+                          int32_t *part_counts, int32_t *part_offsets,
+                          int32_t *slot_of, int32_t *src_token, int32_t *src_k,
+                          void *recv, float *recv_scales, float *recv_w,
+                          void *workspace, size_t workspace_bytes,
+                          uint32_t *err_flags, ep_stream_t stream);
+
+/*
  * ep_combine -- weighted top-k reduce of expert outputs back to token order.
  *
  * In:  y        bf16 [R, H] expert outputs in the receive layout, 16-byte

@@ -372,3 +372,75 @@ def test_out_of_range_slots_are_skipped_and_flagged():
     assert int(plan.layout_out.err_flags.item()) == ep.ERRF_BAD_SLOT
     o = oracle.combine(y, w, np.where((slot >= 0) & (slot < plan.R), slot, -1).astype(np.int32))
     assert_combine_close(bits(out), o)
+
+
+# ------------------------------------------------- fused layout + dispatch
+
+FUSED_CASES = [
+    # (T, H, E, k, P, capacity or None, fp8, mask_frac, duplicates)
+    (128, 7168, 256, 8, 32, 128, True, 0.0, False),      # decode-shaped
+    (128, 1024, 16, 4, 1, None, False, 0.0, False),      # tiny-shaped
+    (1, 128, 4, 1, 1, None, True, 0.0, False),
+    (3, 8, 4, 4, 2, 1, False, 0.2, True),                # capacity overflow, masks, duplicates
+    (200, 384, 64, 6, 8, None, True, 0.1, False),        # fp8 scales stored per element
+    (64, 4104, 1024, 32, 16, None, False, 0.0, False),   # k = 32, E = 1024, odd row size
+    (256, 7168, 256, 8, 32, None, True, 0.0, False),     # N = 2048, the fused limit
+    (300, 7168, 256, 8, 32, None, True, 0.0, False),     # beyond it: the two-call path
+    (17, 2048, 32, 8, 4, 3, False, 0.05, True),
+]
+
+
+@pytest.mark.parametrize("T,H,E,k,P,cap,fp8,mask,dup", FUSED_CASES)
+def test_layout_dispatch_matches_oracle(T, H, E, k, P, cap, fp8, mask, dup):
+    rng = np.random.default_rng(T * 13 + H + E)
+    if dup:
+        idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    else:
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < mask] = -1
+    if T >= 3:
+        idx[1, 0] = E + 3                                    # a bad id: flagged, treated as masked
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32) * 2)
+    w = rng.random((T, k)).astype(np.float32)
+    wl = W.Workload("f", T=T, H=H, E=E, k=k, P=P, routing="uniform", fp8=fp8,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    plan = plan_for(wl, with_weights=True)
+    plan.recv.view(torch.uint8).fill_(0x33)
+    plan.recv_w.fill_(-1.0)
+    L, recv, scales, recv_w = plan.layout_dispatch(dev(idx), bf16_dev(x), dev(w))
+    torch.cuda.synchronize()
+    g = {key: getattr(L, key).cpu().numpy() for key in
+         ("counts", "offsets", "part_counts", "part_offsets", "slot_of", "src_token", "src_k")}
+    g["err"] = int(L.err_flags.cpu().numpy().view(np.uint32)[0])
+    o = oracle_layout(wl, idx)
+    assert_layout_equal(g, o)
+    live = np.zeros(wl.R, bool)
+    live[o["slot_of"][o["slot_of"] >= 0]] = True
+    raw = recv.view(torch.uint8).cpu().numpy().reshape(wl.R, -1)
+    if fp8:
+        oq, os_, ow = oracle.dispatch_fp8(x, o["slot_of"], wl.R, w)
+        np.testing.assert_array_equal(raw[live], oq[live])
+        np.testing.assert_array_equal(scales.cpu().numpy()[live].view(np.uint32), os_[live].view(np.uint32))
+    else:
+        orecv, ow = oracle.dispatch_bf16(x, o["slot_of"], wl.R, w)
+        np.testing.assert_array_equal(raw[live].view(np.uint16), orecv[live])
+    assert (raw[~live] == 0x33).all()
+    np.testing.assert_array_equal(recv_w.cpu().numpy()[live], ow[live])
+    assert (recv_w.cpu().numpy()[~live] == -1.0).all()
+
+
+@pytest.mark.parametrize("name", ["decode", "tiny"])
+def test_layout_dispatch_workloads_equal_separate_calls(name):
+    d = W.make(name)
+    wl = d["wl"]
+    a, b = plan_for(wl), plan_for(wl)
+    La, ra, sa, _ = a.layout_dispatch(dev(d["topk_idx"]), bf16_dev(d["x"]))
+    Lb = b.layout(dev(d["topk_idx"]))
+    rb, sb, _ = b.dispatch(bf16_dev(d["x"]))
+    torch.cuda.synchronize()
+    for key in ("counts", "offsets", "part_counts", "part_offsets", "slot_of", "src_token", "src_k", "err_flags"):
+        assert torch.equal(getattr(La, key), getattr(Lb, key)), key
+    live = La.slot_of.flatten().long()
+    assert torch.equal(ra.view(torch.uint8)[live], rb.view(torch.uint8)[live])
+    if sa is not None:
+        assert torch.equal(sa[live], sb[live])
