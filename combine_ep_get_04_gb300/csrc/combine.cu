@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t first = blockIdx.x;
+    pdl_launch_dependents();
     if (first >= a.units) return;
     const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
 
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
 
     bool ok = true;
     if (warp == 0) {
@@ -229,14 +231,12 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
     cudaError_t err = resident(combine_kernel<1>, 1, smem, ctas);
     if (err != cudaSuccess) return err;
     if (a.units <= ctas) {
-        combine_kernel<1><<<(unsigned)a.units, kThreads, smem, stream>>>(a);
-        return cudaGetLastError();
+        return launch_kernel(true, combine_kernel<1>, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
     }
     err = resident(combine_kernel<kStages>, kStages, smem, ctas);
     if (err != cudaSuccess) return err;
     const int64_t grid = ctas < a.units ? ctas : a.units;
-    combine_kernel<kStages><<<(unsigned)grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(false, combine_kernel<kStages>, dim3((unsigned)grid), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace ep

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
     unsigned char* stages = smem + 128;
     const int lane = threadIdx.x;
     const int64_t first = blockIdx.x;
+    pdl_launch_dependents();
     if (first >= a.units) return;
     const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
 
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
         fence_mbar_init();
     }
     __syncwarp();
+    pdl_wait();
 
     auto issue_load = [&](int64_t i) {
         const int64_t u = first + i * gridDim.x;
@@ -164,6 +166,7 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t first = blockIdx.x;
+    pdl_launch_dependents();
     if (first >= a.units) return;
     const int64_t n_mine = (a.units - 1 - first) / gridDim.x + 1;
     const uint32_t in_bytes = (uint32_t)a.nblk * 256u;
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
 
     auto issue_load = [&](int64_t i) {
         const int64_t u = first + i * gridDim.x;
@@ -307,8 +311,7 @@ cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStrea
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms * per_sm;
     if (grid > a.units) grid = a.units;
-    kern<<<(unsigned)grid, 32, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(grid >= a.units, kern, dim3((unsigned)grid), dim3(32), smem, stream, a);
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream_t stream) {
@@ -342,8 +345,7 @@ cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms * per_sm;
     if (grid > a.units) grid = a.units;
-    kern<<<(unsigned)grid, kFp8Threads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(grid >= a.units, kern, dim3((unsigned)grid), dim3(kFp8Threads), smem, stream, a);
 }
 
 }  // namespace ep

@@ -120,6 +120,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Lets the next kernel of the stream (launched with programmatic stream
+// serialization) start its prologue once every CTA of this grid got here.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the previous grid of the stream has completed and its memory
+// is visible.  Returns at once when there is no such grid.  Every global
+// read or write that may touch that grid's data comes after this.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- bf16
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

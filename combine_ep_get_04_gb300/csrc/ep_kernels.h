@@ -9,6 +9,27 @@
 
 namespace ep {
 
+// Launches `kern`; with pdl, under programmatic stream serialization: it may
+// begin while the previous kernel of the stream finishes, and waits
+// (pdl_wait) before it touches global memory.  Used for latency-sized grids
+// (about one unit of work per CTA), where the launch gap is a large share of
+// the time; large persistent grids launch normally.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Sets the text ep_last_error() returns on the calling thread.
 void record_last_error(const char* msg);
 

@@ -44,7 +44,9 @@ static_assert(kLayoutChunk == kThreads, "one chunk entry per thread");
 __global__ void __launch_bounds__(kThreads) layout_hist_kernel(const int32_t* __restrict__ idx, int N, int E,
                                                                int32_t* __restrict__ hist) {
     extern __shared__ int32_t cnt_s[];
+    pdl_launch_dependents();
     for (int e = threadIdx.x; e < E; e += kThreads) cnt_s[e] = 0;
+    pdl_wait();
     const int n = blockIdx.x * kThreads + threadIdx.x;
     int e = -1;
     if (n < N) {
@@ -77,12 +79,14 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(LayoutParams p) {
     const int N = (int)p.N;
     const bool ranks_chunk = c < p.num_chunks;
 
+    pdl_launch_dependents();
     if (tid == 0) flags_s = 0;
     for (int e = tid; e < E; e += kThreads) { base_s[e] = 0; cnt_s[e] = 0; }
     if (ranks_chunk) {
         for (int i = tid; i < kWarps * E; i += kThreads) tab[i] = 0;
     }
     __syncthreads();
+    pdl_wait();
 
     // 1. This thread's entry of the chunk (my_e, its rank inside the warp),
     //    the per-warp counts of the chunk (tab), the totals and the copies
@@ -287,9 +291,8 @@ cudaError_t launch_layout(const LayoutParams& p_in, int num_sms, cudaStream_t st
                                            (int)smem);
     if (err != cudaSuccess) return err;
     if (p.hist != nullptr) {
-        layout_hist_kernel<<<p.num_chunks, kThreads, p.E * sizeof(int32_t), stream>>>(p.topk_idx, (int)p.N, p.E,
-                                                                                     p.hist);
-        err = cudaGetLastError();
+        err = launch_kernel(false, layout_hist_kernel, dim3(p.num_chunks), dim3(kThreads), p.E * sizeof(int32_t), stream,
+                         p.topk_idx, (int)p.N, p.E, p.hist);
         if (err != cudaSuccess) return err;
     }
     // In capacity mode the unused rows are marked per expert; spread that over
@@ -300,8 +303,10 @@ cudaError_t launch_layout(const LayoutParams& p_in, int num_sms, cudaStream_t st
     if (fill_ctas > grid) grid = fill_ctas < 8 ? fill_ctas : 8;
     if (grid < p.num_chunks) grid = p.num_chunks;
     (void)num_sms;
-    layout_rank_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    // The rank kernel is latency-sized (about one CTA per 1024 ids): let it
+    // start while the histogram kernel (or the caller's previous kernel)
+    // finishes.
+    return launch_kernel(true, layout_rank_kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, p);
 }
 
 }  // namespace ep

@@ -79,6 +79,12 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
     const int sl = u - t * a.slices;
     const int tk0 = t * a.k;
 
+    pdl_launch_dependents();
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    pdl_wait();
     // All loads of routing ids are issued at once, before anything waits.
     int ids[kIdsPerThread];
 #pragma unroll
@@ -92,8 +98,6 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         if (my_tok_e < -1 || my_tok_e >= a.E) my_tok_e = -1;
     }
     if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
         misc_s[0] = 0;
         misc_s[1] = 0;
     }
@@ -377,8 +381,7 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
                                            (int)smem);
     if (err != cudaSuccess) return err;
     const int64_t units = (int64_t)f.T * a.slices;
-    layout_dispatch_kernel<<<(unsigned)(units + 1), kThreadsF, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(true, layout_dispatch_kernel, dim3((unsigned)(units + 1)), dim3(kThreadsF), smem, stream, a);
 }
 
 }  // namespace ep
