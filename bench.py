@@ -81,23 +81,32 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+KERNEL_SOURCES = {
+    "layout": ("layout.cu",),
+    "dispatch": ("dispatch.cu",),
+    "layout_dispatch": ("layout_dispatch.cu",),
+    "combine": ("combine.cu",),
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """Digest of the sources a kernel is built from (its .cu plus the shared
+    device header and launch declarations)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_ep_get_04_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel] + ("ep_device.cuh", "ep_kernels.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str, kernel: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (profiles/traffic.txt)."""
+    """DRAM bytes (read + write) per call of a kernel stage from the committed
+    ncu summary profiles/traffic.txt, if it was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split("#", 1)[0].split()
