@@ -151,15 +151,23 @@ struct Fp8Args {
     uint32_t out_stride;     // bytes per output stage: nblk*128 q + nblk*4 scales, rounded to 128
 };
 
-constexpr int kFp8Warps = 8;
-constexpr int kFp8Threads = kFp8Warps * 32;
-constexpr int kFp8OutStages = 2;
+constexpr int kFp8QuantWarps = 8;
+constexpr int kFp8Threads = (2 + kFp8QuantWarps) * 32;   // producer, storer, quantisers
+constexpr int kFp8OutStages = 3;
 
-// Warp 0 issues loads (lane 0) and the k stores (lane j); all warps quantise.
-template <int NS>
+// Warp-specialised: warp 0 (lane 0) fills a ring of NS input stages with bulk
+// copies of x; warps 2.. quantise a unit from its input stage into one of NSO
+// output stages (codes, then scales) and arrive on that stage's "full"
+// barrier; warp 1 issues the k bulk stores of each finished output stage (lane
+// j: copy j) and hands a stage back once its stores have read it.  No
+// block-wide barrier inside the loop.
+template <int NS, int NSO>
 __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* in_full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* in_empty = in_full + NS;
+    uint64_t* out_full = in_empty + NS;
+    uint64_t* out_empty = out_full + NSO;
     unsigned char* in_st = smem + 128;
     unsigned char* out_st = in_st + (size_t)NS * a.in_stride;
     const int tid = threadIdx.x;
@@ -174,56 +182,115 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
 
     if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&in_full[s], 1);
+            mbar_init(&in_empty[s], kFp8QuantWarps);
+        }
+#pragma unroll
+        for (int o = 0; o < NSO; ++o) {
+            mbar_init(&out_full[o], kFp8QuantWarps);
+            mbar_init(&out_empty[o], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
     pdl_wait();
 
-    auto issue_load = [&](int64_t i) {
-        const int64_t u = first + i * gridDim.x;
-        const int64_t t = u / a.slices;
-        const int sl = (int)(u - t * a.slices);
-        const int s = (int)(i % NS);
-        mbar_arrive_expect_tx(&bars[s], in_bytes);
-        bulk_load(in_st + (size_t)s * a.in_stride,
-                  a.x + (t * a.H + (int64_t)sl * a.nblk * 128) * 2, in_bytes, &bars[s]);
-    };
-    if (tid == 0) {
-        for (int64_t i = 0; i < NS - 1 && i < n_mine; ++i) issue_load(i);
+    bool ok = true;
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            int64_t i = 0;
+            for (; i < n_mine; ++i) {
+                const int s = (int)(i % NS);
+                if (i >= NS && !mbar_wait(&in_empty[s], (uint32_t)(((i / NS) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int64_t u = first + i * gridDim.x;
+                const int64_t t = u / a.slices;
+                const int sl = (int)(u - t * a.slices);
+                mbar_arrive_expect_tx(&in_full[s], in_bytes);
+                bulk_load(in_st + (size_t)s * a.in_stride, a.x + (t * a.H + (int64_t)sl * a.nblk * 128) * 2,
+                          in_bytes, &in_full[s]);
+            }
+            if (!ok) {
+                // copies already issued target this CTA's shared memory: let
+                // them land (each wait bounded) before the CTA exits
+                for (int64_t r = (i > NS ? i - NS : 0); r < i; ++r) {
+                    (void)mbar_wait(&in_full[r % NS], (uint32_t)((r / NS) & 1));
+                }
+                if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+            }
+        }
+        return;
     }
 
-    bool ok = true;
-    int64_t i = 0;
-    for (; i < n_mine; ++i) {
-        const int64_t u = first + i * gridDim.x;
-        const int64_t t = u / a.slices;
-        const int sl = (int)(u - t * a.slices);
-        const int s = (int)(i % NS);
-        unsigned char* ob = out_st + (size_t)(i % kFp8OutStages) * a.out_stride;
-        float* oscale = reinterpret_cast<float*>(ob + q_bytes);
-
-        // Output stage i%2 was read by the stores of unit i-2.
-        if (warp == 0 && i >= kFp8OutStages) bulk_wait_read<kFp8OutStages - 1>();
-        __syncthreads();
-        // Input stage (i+NS-1)%NS was last read while quantising unit i-1.
-        if (tid == 0 && i + NS - 1 < n_mine) issue_load(i + NS - 1);
-
-        int32_t slot = -1;
-        float w = 0.f;
-        if (warp == 0 && lane < a.k) {
-            slot = __ldg(a.slot_of + t * a.k + lane);
+    if (warp == 1) {
+        // -------------------------------------------------------- storer
+        // Lane j holds the slot (and weight) of copy j, loaded one unit ahead.
+        auto load_index = [&](int64_t i, int32_t& slot, float& w) {
+            const int64_t t = (first + i * gridDim.x) / a.slices;
+            slot = -1;
+            w = 0.f;
+            if (lane < a.k) {
+                slot = __ldg(a.slot_of + t * a.k + lane);
+                if (a.recv_w != nullptr) w = __ldg(a.topk_w + t * a.k + lane);
+            }
+        };
+        int32_t next_slot;
+        float next_w;
+        load_index(0, next_slot, next_w);
+        for (int64_t i = 0; i < n_mine; ++i) {
+            const int o = (int)(i % NSO);
+            const int64_t u = first + i * gridDim.x;
+            const int64_t t = u / a.slices;
+            const int sl = (int)(u - t * a.slices);
+            int32_t slot = next_slot;
+            const float w = next_w;
+            if (i + 1 < n_mine) load_index(i + 1, next_slot, next_w);
             if (slot < -1 || slot >= a.R) {
                 if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
                 slot = -1;
             }
-            if (a.recv_w != nullptr && sl == 0 && slot >= 0) w = __ldg(a.topk_w + t * a.k + lane);
+            ok = __all_sync(kFull, mbar_wait(&out_full[o], (uint32_t)((i / NSO) & 1)));
+            if (!ok) break;
+            const unsigned char* ob = out_st + (size_t)o * a.out_stride;
+            const float* oscale = reinterpret_cast<const float*>(ob + q_bytes);
+            if (slot >= 0) {
+                bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, ob, q_bytes);
+                float* sdst = a.recv_s + (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
+                if (a.scale_bulk) {
+                    bulk_store(sdst, oscale, (uint32_t)a.nblk * 4u);
+                } else {
+                    for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
+                }
+                if (a.recv_w != nullptr && sl == 0) a.recv_w[slot] = w;
+            }
+            bulk_commit();
+            if (i >= 1) {   // the stores of unit i-1 have read their stage: hand it back
+                bulk_wait_read<1>();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&out_empty[(i - 1) % NSO]);
+            }
         }
-        ok = __syncthreads_and(mbar_wait(&bars[s], (uint32_t)((i / NS) & 1))) != 0;
-        if (!ok) break;
+        bulk_wait_all();
+        if (!ok && lane == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+        return;
+    }
 
+    // ------------------------------------------------------------ quantisers
+    const int qw = warp - 2;
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = (int)(i % NS);
+        const int o = (int)(i % NSO);
+        ok = __all_sync(kFull, mbar_wait(&in_full[s], (uint32_t)((i / NS) & 1)));
+        if (ok && i >= NSO) ok = __all_sync(kFull, mbar_wait(&out_empty[o], (uint32_t)(((i / NSO) - 1) & 1)));
+        if (!ok) break;
         const unsigned char* ib = in_st + (size_t)s * a.in_stride;
-        for (int b = warp; b < a.nblk; b += kFp8Warps) {
+        unsigned char* ob = out_st + (size_t)o * a.out_stride;
+        float* oscale = reinterpret_cast<float*>(ob + q_bytes);
+        for (int b = qw; b < a.nblk; b += kFp8QuantWarps) {
             const uint2 v = *reinterpret_cast<const uint2*>(ib + b * 256 + lane * 8);
             const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
             float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
@@ -236,29 +303,13 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
             if (lane == 0) oscale[b] = sc;
         }
         fence_proxy_async_smem();
-        __syncthreads();
-
-        if (warp == 0) {
-            if (slot >= 0) {
-                bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, ob, q_bytes);
-                float* sdst = a.recv_s + (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
-                if (a.scale_bulk) {
-                    bulk_store(sdst, oscale, (uint32_t)a.nblk * 4u);
-                } else {
-                    for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
-                }
-                if (a.recv_w != nullptr && sl == 0) a.recv_w[slot] = w;
-            }
-            bulk_commit();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&in_empty[s]);
+            mbar_arrive(&out_full[o]);
         }
     }
-    if (warp == 0) bulk_wait_all();
-    if (!ok && tid == 0) {
-        for (int64_t r = i; r < i + NS - 1 && r < n_mine; ++r) {
-            (void)mbar_wait(&bars[r % NS], (uint32_t)((r / NS) & 1));
-        }
-        if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
-    }
+    if (!ok && lane == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
 }
 
 // Number of slices a row of n granules is cut into: the smallest divisor d of
@@ -336,7 +387,7 @@ cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream
     a.out_stride = ((uint32_t)a.nblk * 132u + 127u) & ~127u;
     a.units = (int64_t)p.T * a.slices;
     const size_t smem = 128 + (size_t)kFp8Stages * a.in_stride + (size_t)kFp8OutStages * a.out_stride;
-    auto kern = dispatch_fp8_kernel<kFp8Stages>;
+    auto kern = dispatch_fp8_kernel<kFp8Stages, kFp8OutStages>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
