@@ -17,15 +17,34 @@
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
+// Pipeline shape (compile-time; the defaults are the tuned values).
+#ifndef EP_COMBINE_STAGES
+#define EP_COMBINE_STAGES 4
+#endif
+#ifndef EP_COMBINE_STAGE_BYTES
+#define EP_COMBINE_STAGE_BYTES 16384
+#endif
+#ifndef EP_COMBINE_CONSUMER_WARPS
+#define EP_COMBINE_CONSUMER_WARPS 4
+#endif
+
 namespace ep {
 
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kConsumerWarps = 4;
+
+// Shared-memory layout of a ring of NS stages: 2*NS mbarriers, NS x 32
+// weights, NS valid-row masks, each region rounded up to 128 bytes, then the
+// stages.
+constexpr uint32_t round128(uint32_t b) { return (b + 127u) / 128u * 128u; }
+constexpr uint32_t weights_offset(int ns) { return round128(16u * ns); }
+constexpr uint32_t mask_offset(int ns) { return weights_offset(ns) + 128u * ns; }
+constexpr uint32_t stages_offset(int ns) { return round128(mask_offset(ns) + 4u * ns); }
+constexpr int kConsumerWarps = EP_COMBINE_CONSUMER_WARPS;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr int kStages = 4;
-constexpr uint32_t kStageBytesMax = 16384;   // k rows x slice bytes per stage
+constexpr int kStages = EP_COMBINE_STAGES;
+constexpr uint32_t kStageBytesMax = EP_COMBINE_STAGE_BYTES;   // k rows x slice bytes per stage
 
 struct Args {
     const unsigned char* y;
@@ -60,9 +79,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                     // [NS] data landed
     uint64_t* empty = full + NS;                                            // [NS] stage free again
-    float* w_s = reinterpret_cast<float*>(smem + 128);                      // [NS][32] weights, 0 if no row
-    uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + 128 + NS * 128);  // [NS] valid-row bits
-    unsigned char* stages = smem + 256 + NS * 128;
+    float* w_s = reinterpret_cast<float*>(smem + weights_offset(NS));       // [NS][32] weights, 0 if no row
+    uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + mask_offset(NS)); // [NS] valid-row bits
+    unsigned char* stages = smem + stages_offset(NS);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -218,7 +237,7 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
     // batches), launch exactly that: every unit starts immediately.  Otherwise
     // a persistent grid of kStages-deep rings.
     auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
-        smem = 256 + (size_t)ns * 128 + (size_t)ns * a.stage_bytes;
+        smem = stages_offset(ns) + (size_t)ns * a.stage_bytes;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         int per_sm = 0;

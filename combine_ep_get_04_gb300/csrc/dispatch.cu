@@ -16,11 +16,38 @@
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
+// Pipeline shape (compile-time; the defaults are the tuned values).
+#ifndef EP_BF16_STAGES
+#define EP_BF16_STAGES 4
+#endif
+#ifndef EP_BF16_LOOKAHEAD
+#define EP_BF16_LOOKAHEAD 2
+#endif
+#ifndef EP_BF16_SLICE_GRANULES
+#define EP_BF16_SLICE_GRANULES 1024   // 16-byte granules per bf16 unit at most
+#endif
+#ifndef EP_FP8_STAGES
+#define EP_FP8_STAGES 3
+#endif
+#ifndef EP_FP8_OUT_STAGES
+#define EP_FP8_OUT_STAGES 3
+#endif
+#ifndef EP_FP8_QUANT_WARPS
+#define EP_FP8_QUANT_WARPS 8
+#endif
+#ifndef EP_FP8_SLICE_BLOCKS
+#define EP_FP8_SLICE_BLOCKS 64        // 128-channel blocks per fp8 unit at most
+#endif
+
 namespace ep {
 
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// Shared-memory header holding a kernel's mbarriers (8 bytes each), rounded
+// up to 128 bytes so that the stages after it stay 128-byte aligned.
+constexpr uint32_t header_bytes(int n_barriers) { return (uint32_t)((n_barriers * 8 + 127) / 128 * 128); }
 
 struct Bf16Args {
     const unsigned char* x;
@@ -44,7 +71,7 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
     static_assert(LA >= 1 && LA <= NS - 1, "lookahead must leave a stage for the stores");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    unsigned char* stages = smem + 128;
+    unsigned char* stages = smem + header_bytes(NS);
     const int lane = threadIdx.x;
     const int64_t first = blockIdx.x;
     pdl_launch_dependents();
@@ -151,9 +178,9 @@ struct Fp8Args {
     uint32_t out_stride;     // bytes per output stage: nblk*128 q + nblk*4 scales, rounded to 128
 };
 
-constexpr int kFp8QuantWarps = 8;
+constexpr int kFp8QuantWarps = EP_FP8_QUANT_WARPS;
 constexpr int kFp8Threads = (2 + kFp8QuantWarps) * 32;   // producer, storer, quantisers
-constexpr int kFp8OutStages = 3;
+constexpr int kFp8OutStages = EP_FP8_OUT_STAGES;
 
 // Warp-specialised: warp 0 (lane 0) fills a ring of NS input stages with bulk
 // copies of x; warps 2.. quantise a unit from its input stage into one of NSO
@@ -168,7 +195,7 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
     uint64_t* in_empty = in_full + NS;
     uint64_t* out_full = in_empty + NS;
     uint64_t* out_empty = out_full + NSO;
-    unsigned char* in_st = smem + 128;
+    unsigned char* in_st = smem + header_bytes(2 * NS + 2 * NSO);
     unsigned char* out_st = in_st + (size_t)NS * a.in_stride;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -330,9 +357,9 @@ int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t 
 
 }  // namespace
 
-constexpr int kBf16Stages = 4;
-constexpr int kBf16Lookahead = 2;
-constexpr int kFp8Stages = 3;
+constexpr int kBf16Stages = EP_BF16_STAGES;
+constexpr int kBf16Lookahead = EP_BF16_LOOKAHEAD;
+constexpr int kFp8Stages = EP_FP8_STAGES;
 
 cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStream_t stream) {
     if (p.T == 0) return cudaSuccess;
@@ -348,11 +375,11 @@ cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStrea
     a.k = p.k;
     // Units of at most 16 KB, at least 1 KB, enough of them for ~4 per SM.
     const int64_t vec16 = a.row_bytes / 16;
-    a.slices = pick_slices(p.T, vec16, 1024, 64, 4LL * num_sms);
+    a.slices = pick_slices(p.T, vec16, EP_BF16_SLICE_GRANULES, 64, 4LL * num_sms);
     a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
     a.stage_stride = (a.slice_bytes + 127u) & ~127u;
     a.units = (int64_t)p.T * a.slices;
-    const size_t smem = 128 + (size_t)kBf16Stages * a.stage_stride;
+    const size_t smem = header_bytes(kBf16Stages) + (size_t)kBf16Stages * a.stage_stride;
     auto kern = dispatch_bf16_kernel<kBf16Stages, kBf16Lookahead>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -380,13 +407,14 @@ cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream
     a.nb = p.H / 128;
     a.k = p.k;
     // Units of at most 64 blocks (16 KB of bf16), enough for ~4 per SM.
-    a.slices = pick_slices(p.T, a.nb, 64, 2, 4LL * num_sms);
+    a.slices = pick_slices(p.T, a.nb, EP_FP8_SLICE_BLOCKS, 2, 4LL * num_sms);
     a.nblk = a.nb / a.slices;
     a.scale_bulk = (a.nb % 4 == 0) && (a.nblk % 4 == 0);
     a.in_stride = (uint32_t)a.nblk * 256u;
     a.out_stride = ((uint32_t)a.nblk * 132u + 127u) & ~127u;
     a.units = (int64_t)p.T * a.slices;
-    const size_t smem = 128 + (size_t)kFp8Stages * a.in_stride + (size_t)kFp8OutStages * a.out_stride;
+    const size_t smem = header_bytes(2 * kFp8Stages + 2 * kFp8OutStages) + (size_t)kFp8Stages * a.in_stride +
+                        (size_t)kFp8OutStages * a.out_stride;
     auto kern = dispatch_fp8_kernel<kFp8Stages, kFp8OutStages>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

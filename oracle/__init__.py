@@ -13,7 +13,9 @@ Functions and the passages they follow (DeepEP web pages):
                    calling NVSHMEM public APIs?", low-latency answer).
   dispatch_*    -- hidden row plus per-128-channel fp32 scales sent once per
                    routed expert ("Pipeline direct NVLink dispatch with
-                   triple-buffered prefetch", Summary).
+                   triple-buffered prefetch", Summary); UE8M0 power-of-two
+                   scales ("Support UE8M0 data format", referenced from
+                   "Redundant atomics in internode_ll").
   combine       -- weighted top-k reduce back to token order, fp32
                    accumulation, bf16 result (same PR, Validation table).
 All of them are pinned (tests/test_oracle_*.py); none is "parity unpinned".
@@ -66,6 +68,8 @@ def _load():
             lib.oracle_dispatch_bf16.argtypes = [ctypes.c_int] * 3 + [vp] * 5
             lib.oracle_dispatch_fp8.restype = None
             lib.oracle_dispatch_fp8.argtypes = [ctypes.c_int] * 3 + [vp] * 6
+            lib.oracle_dispatch_fp8_ue8m0.restype = None
+            lib.oracle_dispatch_fp8_ue8m0.argtypes = [ctypes.c_int] * 3 + [vp] * 6
             lib.oracle_combine.restype = None
             lib.oracle_combine.argtypes = [ctypes.c_int] * 3 + [vp] * 4
             lib.oracle_e4m3_encode_n.restype = None
@@ -146,6 +150,31 @@ def dispatch_fp8(x: np.ndarray, slot_of: np.ndarray, R: int, topk_w: np.ndarray 
     _load().oracle_dispatch_fp8(T, H, k, _ptr(x), _ptr(slot_of), _ptr(w), _ptr(recv_q),
                                 _ptr(recv_s), _ptr(recv_w))
     return recv_q, recv_s, recv_w
+
+
+def dispatch_fp8_ue8m0(x: np.ndarray, slot_of: np.ndarray, R: int, topk_w: np.ndarray | None = None):
+    """Returns (recv_q [R, H] uint8 e4m3 codes, recv_e [R, H/128] uint8 biased exponents, recv_w)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = x.shape
+    if H % 128:
+        raise ValueError("fp8 dispatch needs H % 128 == 0")
+    k = slot_of.shape[1]
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    recv_q = np.zeros((R, H), np.uint8)
+    recv_e = np.zeros((R, H // 128), np.uint8)
+    recv_w = None
+    w = None
+    if topk_w is not None:
+        w = np.ascontiguousarray(topk_w, dtype=np.float32)
+        recv_w = np.zeros(R, np.float32)
+    _load().oracle_dispatch_fp8_ue8m0(T, H, k, _ptr(x), _ptr(slot_of), _ptr(w), _ptr(recv_q), _ptr(recv_e),
+                                      _ptr(recv_w))
+    return recv_q, recv_e, recv_w
+
+
+def ue8m0_value(e: np.ndarray) -> np.ndarray:
+    """Scale values of UE8M0 exponent bytes: 2^(e - 127)."""
+    return np.ldexp(1.0, np.asarray(e, dtype=np.int64) - 127)
 
 
 def combine(y: np.ndarray, topk_w: np.ndarray, slot_of: np.ndarray) -> np.ndarray:

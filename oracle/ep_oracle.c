@@ -295,6 +295,55 @@ void oracle_dispatch_fp8(int T, int H, int k, const uint16_t *x,
     }
 }
 
+/*
+ * fp8 dispatch with UE8M0 scales (an unsigned 8-bit exponent: the scale is a
+ * power of two; "Redundant atomics in internode_ll" cross-references PR
+ * "Support UE8M0 data format").  Per token t and block b:
+ *   v  = max(amax, 1e-4) / 448               (fp32 division, round to nearest),
+ *   s  = the smallest power of two >= v,
+ *   q_i = e4m3(x[t,i] / s)                   (exact: s is a power of two),
+ * recv_e[slot, b] = biased exponent of s (s = 2^(recv_e - 127)).
+ */
+void oracle_dispatch_fp8_ue8m0(int T, int H, int k, const uint16_t *x,
+                               const int32_t *slot_of, const float *topk_w,
+                               uint8_t *recv_q, uint8_t *recv_e, float *recv_w)
+{
+    int nb = H / 128;
+    uint8_t q[128];
+    for (int t = 0; t < T; ++t) {
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t *xb = x + (long)t * H + (long)b * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float a = fabsf(bf16_bits_to_f32(xb[i]));
+                if (a > amax) amax = a;
+            }
+            float v = ((amax > 1e-4f) ? amax : 1e-4f) / 448.0f;
+            int ev;
+            float mant = frexpf(v, &ev);          /* v = mant * 2^ev, mant in [0.5, 1) */
+            float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev);
+            int es;
+            (void)frexpf(s, &es);                 /* s = 0.5 * 2^es = 2^(es-1) */
+            uint8_t e8 = (uint8_t)(es - 1 + 127);
+            for (int i = 0; i < 128; ++i) {
+                q[i] = oracle_e4m3_encode(bf16_bits_to_f32(xb[i]) / s);
+            }
+            for (int j = 0; j < k; ++j) {
+                long slot = slot_of[(long)t * k + j];
+                if (slot < 0) continue;
+                memcpy(recv_q + slot * H + (long)b * 128, q, 128);
+                recv_e[slot * nb + b] = e8;
+            }
+        }
+        if (topk_w && recv_w) {
+            for (int j = 0; j < k; ++j) {
+                long slot = slot_of[(long)t * k + j];
+                if (slot >= 0) recv_w[slot] = topk_w[(long)t * k + j];
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Combine                                                              */
 /* ------------------------------------------------------------------ */

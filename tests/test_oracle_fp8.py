@@ -208,3 +208,36 @@ def test_fp8_matches_exact_rational_definition():
             assert Fraction(float(s[t, b])) == s_exact
             for i in range(128):
                 assert q[t, b * 128 + i] == _e4m3_exact(_rn32(Fraction(float(blk[i])) / s_exact)), (t, b, i)
+
+
+# ---- UE8M0 (power-of-two) scales ----
+
+def test_golden_ue8m0_examples():
+    for amax, e8, x, code in read_golden_rows("ue8m0_examples.txt"):
+        xs = np.zeros((1, 128), np.float32)
+        xs[0, 0] = float(amax)
+        xs[0, 1] = float(x)
+        q, e, _ = oracle.dispatch_fp8_ue8m0(W.to_bf16_bits(xs), np.array([[0]], np.int32), 1)
+        assert e[0, 0] == int(e8), (amax, e[0, 0])
+        assert q[0, 1] == int(code, 16), (amax, x, hex(q[0, 1]))
+
+
+def test_ue8m0_scale_properties_and_codes_match_torch():
+    """s is a power of two with v <= s < 2v; codes equal torch's e4m3 of x/s."""
+    rng = np.random.default_rng(17)
+    T, H = 64, 1024
+    xf = (rng.standard_normal((T, H // 128, 128)) * np.exp(rng.uniform(-14, 10, (T, H // 128, 1)))).reshape(T, H)
+    xf = xf.astype(np.float32)
+    xf[3, :128] = 0.0
+    x = W.to_bf16_bits(xf)
+    q, e, _ = oracle.dispatch_fp8_ue8m0(x, np.arange(T, dtype=np.int32)[:, None], T)
+    q32, s32, _ = oracle.dispatch_fp8(x, np.arange(T, dtype=np.int32)[:, None], T)
+    s = oracle.ue8m0_value(e)                                     # float64, exact powers of two
+    v = s32.astype(np.float64)                                    # RN32(max(amax,1e-4)/448)
+    assert (s >= v).all() and (s < 2 * v).all()
+    assert (np.frexp(s)[0] == 0.5).all()
+    xr = oracle.bf16_to_f32(x).astype(np.float64)
+    quot = (xr / np.repeat(s, 128, axis=1)).astype(np.float32)     # exact: s is a power of two
+    assert (np.abs(quot) <= 448.0).all()
+    np.testing.assert_array_equal(q, _torch_e4m3(quot))
+    assert (q[3, :128] == 0).all() and e[3, 0] == 105

@@ -32,6 +32,9 @@ MUTATIONS = {
     "fp8 no saturation": ("return (uint8_t)(sign | 0x7E);", "return (uint8_t)(sign | 0x7F);"),
     "fp8 wrong block scale": ("recv_s[slot * nb + b] = s;", "recv_s[slot * nb + (b + 1) % nb] = s;"),
     "bf16 rounds ties up": ("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
+    "ue8m0 rounds the scale down": ("float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev);",
+                                    "float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev - 1);"),
+    "ue8m0 exponent bias": ("uint8_t e8 = (uint8_t)(es - 1 + 127);", "uint8_t e8 = (uint8_t)(es + 127);"),
 }
 
 CHECKS = [
@@ -42,6 +45,8 @@ CHECKS = [
     "pf.test_golden_fp8_examples",
     "pf.test_midpoints_and_neighbours_match_torch",
     "pf.test_saturation_by_definition",
+    "pf.test_golden_ue8m0_examples",
+    "pf.test_ue8m0_scale_properties_and_codes_match_torch",
     "pf.test_fp8_dispatch_error_bound_and_amax_code",
     "pc.test_golden_combine_example",
     "pc.test_combine_against_fp64_within_bound",
@@ -56,7 +61,7 @@ lib_path, checks = sys.argv[1], json.loads(sys.argv[2])
 if lib_path:
     real = oracle._load()
     mutant = ctypes.CDLL(lib_path)
-    for fn in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_combine",
+    for fn in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_dispatch_fp8_ue8m0", "oracle_combine",
                "oracle_e4m3_encode_n", "oracle_f32_to_bf16_n", "oracle_e4m3_value"):
         getattr(mutant, fn).restype = getattr(real, fn).restype
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
