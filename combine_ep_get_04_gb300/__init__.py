@@ -23,10 +23,10 @@ from dataclasses import dataclass
 import torch
 
 from ._lib import (CAPACITY, ERRF_BAD_EXPERT, ERRF_BAD_SLOT, ERRF_CAPACITY, ERRF_TIMEOUT, EXPORTED, MAX_EXPERTS, MAX_TOPK,
-                   PACKED, PAYLOAD_BF16, PAYLOAD_FP8_E4M3, EPError, Shape, check, library_path, load)
+                   PACKED, PAYLOAD_BF16, PAYLOAD_FP8_E4M3, PAYLOAD_FP8_E4M3_UE8M0, EPError, Shape, check, library_path, load)
 
 __all__ = ["Plan", "Layout", "Shape", "EPError", "get_layout", "dispatch", "combine", "load", "library_path",
-           "PACKED", "CAPACITY", "PAYLOAD_BF16", "PAYLOAD_FP8_E4M3", "ERRF_BAD_EXPERT", "ERRF_CAPACITY",
+           "PACKED", "CAPACITY", "PAYLOAD_BF16", "PAYLOAD_FP8_E4M3", "PAYLOAD_FP8_E4M3_UE8M0", "ERRF_BAD_EXPERT", "ERRF_CAPACITY",
            "ERRF_TIMEOUT", "ERRF_BAD_SLOT", "MAX_EXPERTS", "MAX_TOPK", "EXPORTED", "make_shape", "recv_rows",
            "layout_workspace_bytes", "fused_layout_dispatch", "FUSED_MAX_N", "FUSED_MAX_T"]
 
@@ -101,11 +101,19 @@ class Plan:
     """
 
     def __init__(self, T: int, H: int, E: int, k: int, num_partitions: int = 1, capacity: int | None = None,
-                 fp8: bool = False, with_weights: bool = False, device: str | torch.device = "cuda"):
+                 fp8: bool = False, with_weights: bool = False, device: str | torch.device = "cuda",
+                 scale_fmt: str = "f32"):
+        """scale_fmt (fp8 only): "f32" scales, or "ue8m0" power-of-two scales
+        stored as biased exponent bytes."""
         load()
+        if scale_fmt not in ("f32", "ue8m0"):
+            raise ValueError(f"scale_fmt must be 'f32' or 'ue8m0', got {scale_fmt!r}")
         self.shape = make_shape(T, H, E, k, num_partitions, capacity)
         self.R = recv_rows(self.shape)
         self.fp8 = fp8
+        self.scale_fmt = scale_fmt
+        self.payload = (PAYLOAD_BF16 if not fp8 else
+                        PAYLOAD_FP8_E4M3_UE8M0 if scale_fmt == "ue8m0" else PAYLOAD_FP8_E4M3)
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         ws = layout_workspace_bytes(self.shape)
@@ -118,7 +126,8 @@ class Plan:
             src_k=torch.empty(self.R, **i32), err_flags=torch.zeros(1, **i32))
         if fp8:
             self.recv = torch.empty((self.R, H), dtype=torch.float8_e4m3fn, device=dev)
-            self.recv_scales = torch.empty((self.R, H // 128), dtype=torch.float32, device=dev)
+            self.recv_scales = torch.empty((self.R, H // 128), device=dev,
+                                           dtype=torch.uint8 if scale_fmt == "ue8m0" else torch.float32)
         else:
             self.recv = torch.empty((self.R, H), dtype=torch.bfloat16, device=dev)
             self.recv_scales = None
@@ -154,7 +163,7 @@ class Plan:
         st = load().ep_dispatch(
             ctypes.byref(s), _ptr(x, torch.bfloat16, "x"),
             _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), _ptr(slot_of, torch.int32, "slot_of", s.T * s.k),
-            PAYLOAD_FP8_E4M3 if self.fp8 else PAYLOAD_BF16, _ptr(self.recv), _ptr(self.recv_scales),
+            self.payload, _ptr(self.recv), _ptr(self.recv_scales),
             _ptr(self.recv_w) if topk_w is not None else None, _ptr(self.layout_out.err_flags), _stream(stream))
         check(st, "ep_dispatch")
         return self.recv, self.recv_scales, self.recv_w
@@ -176,7 +185,7 @@ class Plan:
             raise ValueError("this plan routes weights: pass topk_w")
         st = load().ep_layout_dispatch(
             ctypes.byref(s), _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(x, torch.bfloat16, "x"),
-            _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), PAYLOAD_FP8_E4M3 if self.fp8 else PAYLOAD_BF16,
+            _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), self.payload,
             _ptr(L.counts), _ptr(L.offsets), _ptr(L.part_counts), _ptr(L.part_offsets), _ptr(L.slot_of),
             _ptr(L.src_token), _ptr(L.src_k), _ptr(self.recv), _ptr(self.recv_scales),
             _ptr(self.recv_w) if topk_w is not None else None, _ptr(self.workspace), self.workspace_bytes,
@@ -184,7 +193,7 @@ class Plan:
         check(st, "ep_layout_dispatch")
         return L, self.recv, self.recv_scales, self.recv_w
 
-    def combine(self, y: torch.Tensor, topk_w: torch.Tensor, stream: torch.cuda.Stream | None = None,
+    def combine(self, y: torch.Tensor, topk_w: torch.Tensor | None, stream: torch.cuda.Stream | None = None,
                 out: torch.Tensor | None = None, slot_of: torch.Tensor | None = None) -> torch.Tensor:
         s = self.shape
         if tuple(y.shape) != (self.R, s.H):

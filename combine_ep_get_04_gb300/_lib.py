@@ -14,6 +14,7 @@ PACKED = 0
 CAPACITY = 1
 PAYLOAD_BF16 = 0
 PAYLOAD_FP8_E4M3 = 1
+PAYLOAD_FP8_E4M3_UE8M0 = 2
 
 ERRF_BAD_EXPERT = 1
 ERRF_CAPACITY = 2

@@ -19,7 +19,7 @@
 
 // Pipeline shape (compile-time; the defaults are the tuned values).
 #ifndef EP_COMBINE_STAGES
-#define EP_COMBINE_STAGES 4
+#define EP_COMBINE_STAGES 3
 #endif
 #ifndef EP_COMBINE_STAGE_BYTES
 #define EP_COMBINE_STAGE_BYTES 16384
@@ -37,10 +37,10 @@ constexpr unsigned kFull = 0xffffffffu;
 // Shared-memory layout of a ring of NS stages: 2*NS mbarriers, NS x 32
 // weights, NS valid-row masks, each region rounded up to 128 bytes, then the
 // stages.
-constexpr uint32_t round128(uint32_t b) { return (b + 127u) / 128u * 128u; }
-constexpr uint32_t weights_offset(int ns) { return round128(16u * ns); }
-constexpr uint32_t mask_offset(int ns) { return weights_offset(ns) + 128u * ns; }
-constexpr uint32_t stages_offset(int ns) { return round128(mask_offset(ns) + 4u * ns); }
+__host__ __device__ constexpr uint32_t round128(uint32_t b) { return (b + 127u) / 128u * 128u; }
+__host__ __device__ constexpr uint32_t weights_offset(int ns) { return round128(16u * ns); }
+__host__ __device__ constexpr uint32_t mask_offset(int ns) { return weights_offset(ns) + 128u * ns; }
+__host__ __device__ constexpr uint32_t stages_offset(int ns) { return round128(mask_offset(ns) + 4u * ns); }
 constexpr int kConsumerWarps = EP_COMBINE_CONSUMER_WARPS;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kStages = EP_COMBINE_STAGES;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
             w = 0.f;
             if (lane < a.k) {
                 slot = __ldg(a.slot_of + t * a.k + lane);
-                w = __ldg(a.topk_w + t * a.k + lane);
+                w = a.topk_w != nullptr ? __ldg(a.topk_w + t * a.k + lane) : 1.0f;
             }
         };
         int32_t next_slot;

@@ -27,7 +27,7 @@
 #define EP_BF16_SLICE_GRANULES 1024   // 16-byte granules per bf16 unit at most
 #endif
 #ifndef EP_FP8_STAGES
-#define EP_FP8_STAGES 3
+#define EP_FP8_STAGES 4
 #endif
 #ifndef EP_FP8_OUT_STAGES
 #define EP_FP8_OUT_STAGES 3
@@ -47,7 +47,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Shared-memory header holding a kernel's mbarriers (8 bytes each), rounded
 // up to 128 bytes so that the stages after it stay 128-byte aligned.
-constexpr uint32_t header_bytes(int n_barriers) { return (uint32_t)((n_barriers * 8 + 127) / 128 * 128); }
+__host__ __device__ constexpr uint32_t header_bytes(int n_barriers) { return (uint32_t)((n_barriers * 8 + 127) / 128 * 128); }
 
 struct Bf16Args {
     const unsigned char* x;
@@ -163,7 +163,7 @@ struct Fp8Args {
     const int32_t* slot_of;
     const float* topk_w;
     unsigned char* recv;     // e4m3 [R, H]
-    float* recv_s;           // [R, H/128]
+    void* recv_s;            // [R, H/128] f32, or u8 exponents with ue8m0
     float* recv_w;
     uint32_t* err_flags;
     int64_t R;               // receive rows
@@ -174,6 +174,7 @@ struct Fp8Args {
     int nblk;                // 128-channel blocks per unit
     int k;
     int scale_bulk;          // scales stored with a bulk copy (16-byte granular)
+    int ue8m0;               // power-of-two scales, stored as exponent bytes
     uint32_t in_stride;      // bytes per input stage (nblk*256, multiple of 128)
     uint32_t out_stride;     // bytes per output stage: nblk*128 q + nblk*4 scales, rounded to 128
 };
@@ -286,10 +287,14 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
             const float* oscale = reinterpret_cast<const float*>(ob + q_bytes);
             if (slot >= 0) {
                 bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, ob, q_bytes);
-                float* sdst = a.recv_s + (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
-                if (a.scale_bulk) {
-                    bulk_store(sdst, oscale, (uint32_t)a.nblk * 4u);
+                const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
+                if (a.ue8m0) {
+                    uint8_t* edst = static_cast<uint8_t*>(a.recv_s) + s0;
+                    for (int b = 0; b < a.nblk; ++b) edst[b] = ob[q_bytes + b];
+                } else if (a.scale_bulk) {
+                    bulk_store(static_cast<float*>(a.recv_s) + s0, oscale, (uint32_t)a.nblk * 4u);
                 } else {
+                    float* sdst = static_cast<float*>(a.recv_s) + s0;
                     for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
                 }
                 if (a.recv_w != nullptr && sl == 0) a.recv_w[slot] = w;
@@ -323,11 +328,17 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
             float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-            const float sc = __fdiv_rn(fmaxf(m, 1e-4f), 448.0f);
+            const float sc = block_scale(m, a.ue8m0 != 0);
             const uint32_t q01 = pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
             const uint32_t q23 = pack_e4m3x2(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
             *reinterpret_cast<uint32_t*>(ob + b * 128 + lane * 4) = q01 | (q23 << 16);
-            if (lane == 0) oscale[b] = sc;
+            if (lane == 0) {
+                if (a.ue8m0) {
+                    ob[q_bytes + b] = ue8m0_byte(sc);
+                } else {
+                    oscale[b] = sc;
+                }
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -400,6 +411,7 @@ cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream
     a.topk_w = p.topk_w;
     a.recv = static_cast<unsigned char*>(p.recv);
     a.recv_s = p.recv_scales;
+    a.ue8m0 = p.ue8m0;
     a.recv_w = p.recv_w;
     a.err_flags = p.err_flags;
     a.R = p.R;

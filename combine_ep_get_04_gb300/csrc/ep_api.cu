@@ -150,20 +150,21 @@ ep_status_t ep_get_layout(const ep_shape_t* shape, const int32_t* topk_idx, int3
 }
 
 ep_status_t ep_dispatch(const ep_shape_t* shape, const void* x, const float* topk_w, const int32_t* slot_of,
-                        int32_t payload, void* recv, float* recv_scales, float* recv_w, uint32_t* err_flags,
+                        int32_t payload, void* recv, void* recv_scales, float* recv_w, uint32_t* err_flags,
                         ep_stream_t stream) {
     ep_status_t st = check_shape(shape);
     if (st != EP_OK) return st;
-    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3)
+    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3 && payload != EP_PAYLOAD_FP8_E4M3_UE8M0)
         return fail(EP_ERR_INVALID_ARG, "payload = %d is not a payload format", payload);
-    const bool fp8 = payload == EP_PAYLOAD_FP8_E4M3;
+    const bool fp8 = payload != EP_PAYLOAD_BF16;
+    const bool ue8m0 = payload == EP_PAYLOAD_FP8_E4M3_UE8M0;
     if (fp8 && shape->H % 128 != 0) return fail(EP_ERR_INVALID_ARG, "fp8 payload needs H %% 128 == 0 (H = %d)", shape->H);
     if (shape->T == 0) return ok();
     if (x == nullptr || slot_of == nullptr || recv == nullptr)
         return fail(EP_ERR_INVALID_ARG, "x / slot_of / recv is NULL");
     if (!aligned16(x) || !aligned16(recv)) return fail(EP_ERR_INVALID_ARG, "x and recv must be 16-byte aligned");
-    if (fp8 && (recv_scales == nullptr || !aligned16(recv_scales)))
-        return fail(EP_ERR_INVALID_ARG, "fp8 payload needs 16-byte aligned recv_scales");
+    if (fp8 && (recv_scales == nullptr || (!ue8m0 && !aligned16(recv_scales))))
+        return fail(EP_ERR_INVALID_ARG, "fp8 payload needs recv_scales (16-byte aligned for f32 scales)");
     if (recv_w != nullptr && topk_w == nullptr) return fail(EP_ERR_INVALID_ARG, "recv_w needs topk_w");
     int num_sms = 0;
     st = device_info(&num_sms);
@@ -175,6 +176,7 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const void* x, const float* top
     p.slot_of = slot_of;
     p.recv = recv;
     p.recv_scales = recv_scales;
+    p.ue8m0 = ue8m0 ? 1 : 0;
     p.recv_w = recv_w;
     p.err_flags = err_flags;
     p.R = rows_of(shape);
@@ -189,7 +191,7 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const void* x, const float* top
 ep_status_t ep_layout_dispatch(const ep_shape_t* shape, const int32_t* topk_idx, const void* x,
                                const float* topk_w, int32_t payload, int32_t* counts, int32_t* offsets,
                                int32_t* part_counts, int32_t* part_offsets, int32_t* slot_of, int32_t* src_token,
-                               int32_t* src_k, void* recv, float* recv_scales, float* recv_w, void* workspace,
+                               int32_t* src_k, void* recv, void* recv_scales, float* recv_w, void* workspace,
                                size_t workspace_bytes, uint32_t* err_flags, ep_stream_t stream) {
     ep_status_t st = check_shape(shape);
     if (st != EP_OK) return st;
@@ -201,9 +203,10 @@ ep_status_t ep_layout_dispatch(const ep_shape_t* shape, const int32_t* topk_idx,
         return ep_dispatch(shape, x, topk_w, slot_of, payload, recv, recv_scales, recv_w, err_flags, stream);
     }
     // The same checks as ep_get_layout and ep_dispatch, before anything is launched.
-    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3)
+    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3 && payload != EP_PAYLOAD_FP8_E4M3_UE8M0)
         return fail(EP_ERR_INVALID_ARG, "payload = %d is not a payload format", payload);
-    const bool fp8 = payload == EP_PAYLOAD_FP8_E4M3;
+    const bool fp8 = payload != EP_PAYLOAD_BF16;
+    const bool ue8m0 = payload == EP_PAYLOAD_FP8_E4M3_UE8M0;
     if (fp8 && shape->H % 128 != 0) return fail(EP_ERR_INVALID_ARG, "fp8 payload needs H %% 128 == 0 (H = %d)", shape->H);
     if (topk_idx == nullptr || slot_of == nullptr || x == nullptr || recv == nullptr)
         return fail(EP_ERR_INVALID_ARG, "topk_idx / slot_of / x / recv is NULL");
@@ -211,8 +214,8 @@ ep_status_t ep_layout_dispatch(const ep_shape_t* shape, const int32_t* topk_idx,
         src_token == nullptr || src_k == nullptr)
         return fail(EP_ERR_INVALID_ARG, "counts / offsets / part_counts / part_offsets / src_token / src_k is NULL");
     if (!aligned16(x) || !aligned16(recv)) return fail(EP_ERR_INVALID_ARG, "x and recv must be 16-byte aligned");
-    if (fp8 && (recv_scales == nullptr || !aligned16(recv_scales)))
-        return fail(EP_ERR_INVALID_ARG, "fp8 payload needs 16-byte aligned recv_scales");
+    if (fp8 && (recv_scales == nullptr || (!ue8m0 && !aligned16(recv_scales))))
+        return fail(EP_ERR_INVALID_ARG, "fp8 payload needs recv_scales (16-byte aligned for f32 scales)");
     if (recv_w != nullptr && topk_w == nullptr) return fail(EP_ERR_INVALID_ARG, "recv_w needs topk_w");
     int num_sms = 0;
     st = device_info(&num_sms);
@@ -242,6 +245,7 @@ ep_status_t ep_layout_dispatch(const ep_shape_t* shape, const int32_t* topk_idx,
     f.mode = shape->mode;
     f.cap = shape->capacity;
     f.fp8 = fp8 ? 1 : 0;
+    f.ue8m0 = ue8m0 ? 1 : 0;
     return launched(ep::launch_layout_dispatch(f, num_sms, reinterpret_cast<cudaStream_t>(stream)),
                     "layout+dispatch launch");
 }
@@ -251,8 +255,8 @@ ep_status_t ep_combine(const ep_shape_t* shape, const void* y, const float* topk
     ep_status_t st = check_shape(shape);
     if (st != EP_OK) return st;
     if (shape->T == 0) return ok();
-    if (y == nullptr || topk_w == nullptr || slot_of == nullptr || out == nullptr)
-        return fail(EP_ERR_INVALID_ARG, "y / topk_w / slot_of / out is NULL");
+    if (y == nullptr || slot_of == nullptr || out == nullptr)
+        return fail(EP_ERR_INVALID_ARG, "y / slot_of / out is NULL");
     if (!aligned16(y) || !aligned16(out)) return fail(EP_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
     int num_sms = 0;
     st = device_info(&num_sms);

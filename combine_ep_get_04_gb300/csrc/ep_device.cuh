@@ -147,6 +147,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Scale of a 128-channel block: v = RN32(max(amax, 1e-4) / 448); with UE8M0
+// scales, the smallest power of two >= v (exact: bump the exponent unless the
+// mantissa is zero; v is a positive normal number here).
+__device__ __forceinline__ float block_scale(float amax, bool ue8m0) {
+    float v = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    if (ue8m0) {
+        uint32_t b = __float_as_uint(v);
+        if (b & 0x007fffffu) b = (b & 0x7f800000u) + 0x00800000u;
+        v = __uint_as_float(b);
+    }
+    return v;
+}
+
+// Biased exponent byte of a power-of-two scale (UE8M0: value 2^(e - 127)).
+__device__ __forceinline__ uint8_t ue8m0_byte(float pow2) { return (uint8_t)(__float_as_uint(pow2) >> 23); }
+
 // Two floats -> packed e4m3x2 (round to nearest even, saturate to +-448),
 // `lo` in the low byte.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {

@@ -69,11 +69,12 @@ struct DispatchParams {
     const float* topk_w;    // [T, k] or nullptr
     const int32_t* slot_of; // [T, k]
     void* recv;             // bf16 or e4m3 [R, H]
-    float* recv_scales;     // [R, H/128] (fp8)
+    void* recv_scales;      // [R, H/128] f32, or u8 exponents with ue8m0 (fp8)
     float* recv_w;          // [R] or nullptr
     uint32_t* err_flags;    // may be nullptr
     int64_t R;              // receive rows
     int T, H, k;
+    int ue8m0;              // power-of-two scales stored as exponent bytes
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStream_t stream);
@@ -96,11 +97,11 @@ struct FusedLaunch {
     int32_t* src_token;
     int32_t* src_k;
     void* recv;
-    float* recv_scales;
+    void* recv_scales;
     float* recv_w;
     uint32_t* err_flags;
     int64_t R;
-    int T, H, E, k, P, mode, cap, fp8;
+    int T, H, E, k, P, mode, cap, fp8, ue8m0;
 };
 
 bool fused_layout_dispatch_fits(int64_t N, int64_t T, int E);

@@ -41,12 +41,13 @@ struct FusedArgs {
     int32_t* src_token;
     int32_t* src_k;
     unsigned char* recv;
-    float* recv_s;
+    void* recv_s;            // f32 scales, or u8 exponents with ue8m0
     float* recv_w;
     uint32_t* err_flags;
     int T, H, E, k, P, mode, cap, N, R;
     int slices;              // units per token row
     int fp8;
+    int ue8m0;               // power-of-two scales stored as exponent bytes
     int nb;                  // H / 128 (fp8)
     int nblk;                // 128-channel blocks per unit (fp8)
     int scale_bulk;          // scale rows stored with a bulk copy
@@ -85,6 +86,10 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         fence_mbar_init();
     }
     pdl_wait();
+    if (tid == 0 && !hist_cta) {   // the slice of x does not depend on the layout: start it first
+        mbar_arrive_expect_tx(bar, a.in_bytes);
+        bulk_load(in_st, a.x + (int64_t)t * a.H * 2 + (int64_t)sl * a.in_bytes, a.in_bytes, bar);
+    }
     // All loads of routing ids are issued at once, before anything waits.
     int ids[kIdsPerThread];
 #pragma unroll
@@ -174,10 +179,6 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         __syncthreads();
         if (tid == 0 && a.err_flags != nullptr && misc_s[1]) atomicOr(a.err_flags, (uint32_t)misc_s[1]);
         return;
-    }
-    if (tid == 0) {   // the slice of x does not depend on the layout: start it now
-        mbar_arrive_expect_tx(bar, a.in_bytes);
-        bulk_load(in_st, a.x + (int64_t)t * a.H * 2 + (int64_t)sl * a.in_bytes, a.in_bytes, bar);
     }
 
     // Slot of copy j of this token, from two counts over all ids:
@@ -287,11 +288,17 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
                 float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
                 for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-                const float sc = __fdiv_rn(fmaxf(m, 1e-4f), 448.0f);
+                const float sc = block_scale(m, a.ue8m0 != 0);
                 const uint32_t q01 = pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
                 const uint32_t q23 = pack_e4m3x2(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
                 *reinterpret_cast<uint32_t*>(out_st + b * 128 + lane * 4) = q01 | (q23 << 16);
-                if (lane == 0) oscale[b] = sc;
+                if (lane == 0) {
+                    if (a.ue8m0) {
+                        out_st[q_bytes + b] = ue8m0_byte(sc);
+                    } else {
+                        oscale[b] = sc;
+                    }
+                }
             }
             fence_proxy_async_smem();
             __syncthreads();
@@ -299,10 +306,14 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
                 const int32_t slot = lane < a.k ? slot_s[lane] : -1;
                 if (slot >= 0) {
                     bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, out_st, q_bytes);
-                    float* sdst = a.recv_s + (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
-                    if (a.scale_bulk) {
-                        bulk_store(sdst, oscale, (uint32_t)a.nblk * 4u);
+                    const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
+                    if (a.ue8m0) {
+                        uint8_t* edst = static_cast<uint8_t*>(a.recv_s) + s0;
+                        for (int b = 0; b < a.nblk; ++b) edst[b] = out_st[q_bytes + b];
+                    } else if (a.scale_bulk) {
+                        bulk_store(static_cast<float*>(a.recv_s) + s0, oscale, (uint32_t)a.nblk * 4u);
                     } else {
+                        float* sdst = static_cast<float*>(a.recv_s) + s0;
                         for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
                     }
                 }
@@ -362,6 +373,7 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
     a.N = f.T * f.k;
     a.R = (int)f.R;
     a.fp8 = f.fp8;
+    a.ue8m0 = f.ue8m0;
     if (f.fp8) {
         a.nb = f.H / 128;
         a.slices = pick_divisor(f.T, a.nb, 64, 2, (int64_t)num_sms);

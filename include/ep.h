@@ -71,7 +71,10 @@ typedef enum {
 /* Payload format of ep_dispatch. */
 typedef enum {
     EP_PAYLOAD_BF16 = 0,      /* recv is bf16 [R, H], a bit copy of x         */
-    EP_PAYLOAD_FP8_E4M3 = 1   /* recv is e4m3 [R, H] plus f32 scales [R, H/128] */
+    EP_PAYLOAD_FP8_E4M3 = 1,  /* recv is e4m3 [R, H] plus f32 scales [R, H/128] */
+    EP_PAYLOAD_FP8_E4M3_UE8M0 = 2 /* e4m3 [R, H] plus power-of-two scales stored
+                                 as u8 biased exponents [R, H/128] (UE8M0:
+                                 scale = 2^(e - 127))                          */
 } ep_payload_t;
 
 /* Bits of the device error word. */
@@ -181,8 +184,14 @@ EP_API ep_status_t ep_get_layout_static(const ep_shape_t *shape, const int32_t *
  *               nearest), q = e4m3(x / s) (fp32 division rounded to nearest,
  *               then nearest e4m3, ties to even, saturating at +-448).
  *               16-byte aligned.
- *      recv_scales f32 [R, H/128] (fp8 only, else ignored): s of each block,
- *               16-byte aligned.
+ *               EP_PAYLOAD_FP8_E4M3_UE8M0: as E4M3 but s is the smallest
+ *               power of two >= max(amax, 1e-4) / 448 (that quotient rounded
+ *               to nearest in fp32), so x / s is exact ("Support UE8M0 data
+ *               format", referenced from "Redundant atomics in
+ *               internode_ll").
+ *      recv_scales (fp8 only, else ignored): E4M3: f32 [R, H/128], s of each
+ *               block, 16-byte aligned; E4M3_UE8M0: u8 [R, H/128], the biased
+ *               exponent e of each block's s = 2^(e - 127).
  *      recv_w   f32 [R] or NULL: recv_w[slot_of[t,j]] = topk_w[t,j]
  *               (needs topk_w).
  * Rows of recv / recv_scales / recv_w that receive no copy are not written.
@@ -190,7 +199,7 @@ EP_API ep_status_t ep_get_layout_static(const ep_shape_t *shape, const int32_t *
  */
 EP_API ep_status_t ep_dispatch(const ep_shape_t *shape, const void *x,
                         const float *topk_w, const int32_t *slot_of,
-                        int32_t payload, void *recv, float *recv_scales,
+                        int32_t payload, void *recv, void *recv_scales,
                         float *recv_w, uint32_t *err_flags, ep_stream_t stream);
 
 /*
@@ -214,7 +223,7 @@ EP_API ep_status_t ep_layout_dispatch(const ep_shape_t *shape, const int32_t *to
                           int32_t *counts, int32_t *offsets,
                           int32_t *part_counts, int32_t *part_offsets,
                           int32_t *slot_of, int32_t *src_token, int32_t *src_k,
-                          void *recv, float *recv_scales, float *recv_w,
+                          void *recv, void *recv_scales, float *recv_w,
                           void *workspace, size_t workspace_bytes,
                           uint32_t *err_flags, ep_stream_t stream);
 
@@ -223,7 +232,8 @@ EP_API ep_status_t ep_layout_dispatch(const ep_shape_t *shape, const int32_t *to
  *
  * In:  y        bf16 [R, H] expert outputs in the receive layout, 16-byte
  *               aligned.
- *      topk_w   f32 [T, k].
+ *      topk_w   f32 [T, k], or NULL for an unweighted sum (weights applied on
+ *               the expert side, e.g. from ep_dispatch's recv_w).
  *      slot_of  i32 [T, k] from ep_get_layout (-1 = skipped; values outside
  *               [-1, R) are skipped and flagged EP_ERRF_BAD_SLOT).
  * Out: out      bf16 [T, H], 16-byte aligned:

@@ -17,7 +17,8 @@ Functions and the passages they follow (DeepEP web pages):
                    scales ("Support UE8M0 data format", referenced from
                    "Redundant atomics in internode_ll").
   combine       -- weighted top-k reduce back to token order, fp32
-                   accumulation, bf16 result (same PR, Validation table).
+                   accumulation, bf16 result (same PR, Validation table);
+                   also over fp8 expert outputs with per-128-channel scales.
 All of them are pinned (tests/test_oracle_*.py); none is "parity unpinned".
 """
 from __future__ import annotations
@@ -70,6 +71,8 @@ def _load():
             lib.oracle_dispatch_fp8.argtypes = [ctypes.c_int] * 3 + [vp] * 6
             lib.oracle_dispatch_fp8_ue8m0.restype = None
             lib.oracle_dispatch_fp8_ue8m0.argtypes = [ctypes.c_int] * 3 + [vp] * 6
+            lib.oracle_combine_fp8.restype = None
+            lib.oracle_combine_fp8.argtypes = [ctypes.c_int] * 3 + [vp, vp, ctypes.c_int, vp, vp, vp]
             lib.oracle_combine.restype = None
             lib.oracle_combine.argtypes = [ctypes.c_int] * 3 + [vp] * 4
             lib.oracle_e4m3_encode_n.restype = None
@@ -186,6 +189,23 @@ def combine(y: np.ndarray, topk_w: np.ndarray, slot_of: np.ndarray) -> np.ndarra
     w = np.ascontiguousarray(topk_w, dtype=np.float32)
     out = np.zeros((T, H), np.uint16)
     _load().oracle_combine(T, H, k, _ptr(y), _ptr(w), _ptr(slot_of), _ptr(out))
+    return out
+
+
+def combine_fp8(yq: np.ndarray, ys: np.ndarray, topk_w: np.ndarray | None, slot_of: np.ndarray) -> np.ndarray:
+    """yq: [R, H] uint8 e4m3 codes; ys: [R, H/128] float32 scales or uint8 UE8M0
+    exponents; returns out [T, H] uint16 (bf16 bits)."""
+    yq = np.ascontiguousarray(yq, dtype=np.uint8)
+    H = yq.shape[1]
+    if H % 128:
+        raise ValueError("fp8 combine needs H % 128 == 0")
+    ue8m0 = ys.dtype == np.uint8
+    ys = np.ascontiguousarray(ys)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    T, k = slot_of.shape
+    w = None if topk_w is None else np.ascontiguousarray(topk_w, dtype=np.float32)
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine_fp8(T, H, k, _ptr(yq), _ptr(ys), int(ue8m0), _ptr(w), _ptr(slot_of), _ptr(out))
     return out
 
 

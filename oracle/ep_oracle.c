@@ -372,6 +372,40 @@ void oracle_combine(int T, int H, int k, const uint16_t *y,
     }
 }
 
+/*
+ * combine of fp8 expert outputs: y is e4m3 [R, H] with one scale per 128
+ * channels, ys [R, H/128] (f32, or UE8M0 exponent bytes when ue8m0 != 0).
+ * Each element is dequantised as v = value(q) * s (fp32 product, rounded to
+ * nearest; value(q) is exact in fp32), then summed as in oracle_combine:
+ * out[t, i] = bf16( sum over valid j of w[t,j] * v ), fp32, increasing j.
+ * topk_w may be NULL (unweighted sum).
+ */
+void oracle_combine_fp8(int T, int H, int k, const uint8_t *y, const void *ys, int ue8m0,
+                        const float *topk_w, const int32_t *slot_of, uint16_t *out)
+{
+    int nb = H / 128;
+    for (int t = 0; t < T; ++t) {
+        for (int i = 0; i < H; ++i) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                long slot = slot_of[(long)t * k + j];
+                if (slot < 0) continue;
+                float s;
+                if (ue8m0) {
+                    s = ldexpf(1.0f, (int)((const uint8_t *)ys)[slot * nb + i / 128] - 127);
+                } else {
+                    s = ((const float *)ys)[slot * nb + i / 128];
+                }
+                float v = (float)oracle_e4m3_value(y[slot * H + i]) * s;
+                float w = topk_w ? topk_w[(long)t * k + j] : 1.0f;
+                float prod = w * v;
+                acc = acc + prod;
+            }
+            out[(long)t * H + i] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
 /* Vector helpers for the tests (elementwise over n values). */
 void oracle_e4m3_encode_n(const float *v, uint8_t *codes, long n)
 {

@@ -444,3 +444,67 @@ def test_layout_dispatch_workloads_equal_separate_calls(name):
     assert torch.equal(ra.view(torch.uint8)[live], rb.view(torch.uint8)[live])
     if sa is not None:
         assert torch.equal(sa[live], sb[live])
+
+
+# ------------------------------------------------------------ UE8M0 scales
+
+@pytest.mark.parametrize("T,H,E,k,cap,fused", [(128, 7168, 256, 8, 128, True), (128, 7168, 256, 8, 128, False),
+                                               (640, 7168, 256, 8, None, False), (9, 384, 8, 3, None, True),
+                                               (70, 512, 16, 8, None, False), (2, 65536, 4, 2, None, False)])
+def test_dispatch_fp8_ue8m0_matches_oracle(T, H, E, k, cap, fused):
+    rng = np.random.default_rng(T + H + 5)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < 0.05] = -1
+    scale = np.exp(rng.uniform(-20, 12, size=(T, H // 128, 1))).astype(np.float32)
+    xf = (rng.standard_normal((T, H // 128, 128)).astype(np.float32) * scale).reshape(T, H)
+    xf[:, :128] = 0.0
+    x = W.to_bf16_bits(xf)
+    wl = W.Workload("u", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=True,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    plan = ep.Plan(T, H, E, k, 1, cap, fp8=True, scale_fmt="ue8m0")
+    plan.recv.view(torch.uint8).fill_(0x5A)
+    plan.recv_scales.fill_(0xEE)
+    if fused:
+        _, q, e, _ = plan.layout_dispatch(dev(idx), bf16_dev(x))
+    else:
+        plan.layout(dev(idx))
+        q, e, _ = plan.dispatch(bf16_dev(x))
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, idx)
+    oq, oe, _ = oracle.dispatch_fp8_ue8m0(x, L["slot_of"], wl.R)
+    live = np.zeros(wl.R, bool)
+    live[L["slot_of"][L["slot_of"] >= 0]] = True
+    gq = q.view(torch.uint8).cpu().numpy()
+    ge = e.cpu().numpy()
+    np.testing.assert_array_equal(gq[live], oq[live])
+    np.testing.assert_array_equal(ge[live], oe[live])
+    assert (gq[~live] == 0x5A).all() and (ge[~live] == 0xEE).all()
+
+
+# ------------------------------------- expert-side weights (unweighted combine)
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_combine_unweighted_matches_oracle_with_unit_weights(name):
+    d = W.make(name)
+    wl = d["wl"]
+    y = W.expert_rows(wl.R, wl.H)
+    plan = plan_for(wl)
+    plan.layout(dev(d["topk_idx"]))
+    out = plan.combine(bf16_dev(y), None)
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, d["topk_idx"])
+    ones = np.ones((wl.T, wl.k), np.float32)
+    assert_combine_close(bits(out), oracle.combine(y, ones, L["slot_of"]))
+
+
+def test_expert_side_weights_round_trip():
+    """dispatch routes recv_w; experts scale rows by it; unweighted combine ~ weighted combine."""
+    d = W.make("tiny")
+    wl = d["wl"]
+    plan = plan_for(wl, with_weights=True)
+    plan.layout(dev(d["topk_idx"]))
+    recv, _, recv_w = plan.dispatch(bf16_dev(d["x"]), dev(d["topk_w"]))
+    y_weighted = (recv.float() * recv_w[:, None]).to(torch.bfloat16)
+    a = plan.combine(y_weighted, None).float().clone()
+    b = plan.combine(recv, dev(d["topk_w"])).float()
+    assert bool(((a - b).abs() <= ATOL + RTOL * b.abs()).all())

@@ -110,3 +110,74 @@ def test_dispatch_bf16_leaves_other_rows_untouched():
     np.testing.assert_array_equal(recv[2], x[1])
     for r in (1, 3, 5):
         assert (recv[r] == 0xBEEF).all()
+
+
+# ---- combine over fp8 expert outputs ----
+
+def _read_fp8_combine_fixture():
+    from conftest import read_golden_rows
+    rows, slots, weights, out = [], None, None, None
+    for r in read_golden_rows("combine_fp8_example.txt"):
+        if r[0] == "slots":
+            slots = np.array([int(v) for v in r[1:]], np.int32).reshape(2, 2)
+        elif r[0] == "weights":
+            weights = np.array([float(v) for v in r[1:]], np.float32).reshape(2, 2)
+        elif r[0] == "out":
+            out = np.array([float(v) for v in r[1:]], np.float64).reshape(2, 2)
+        else:
+            rows.append((int(r[0]), float(r[1]), int(r[2], 16), int(r[3], 16)))
+    yq = np.zeros((3, 128), np.uint8)
+    ys = np.zeros((3, 1), np.float32)
+    for row, sc, c0, c1 in rows:
+        yq[row, 0], yq[row, 1], ys[row, 0] = c0, c1, sc
+    return yq, ys, slots, weights, out
+
+
+def test_golden_combine_fp8_example():
+    yq, ys, slots, w, expect = _read_fp8_combine_fixture()
+    got = oracle.bf16_to_f32(oracle.combine_fp8(yq, ys, w, slots))[:, :2]
+    np.testing.assert_array_equal(got.astype(np.float64), expect)
+    # the same scales as UE8M0 exponents give the same result (they are powers of two)
+    e8 = (np.log2(ys).astype(np.int64) + 127).astype(np.uint8)
+    got8 = oracle.bf16_to_f32(oracle.combine_fp8(yq, e8, w, slots))[:, :2]
+    np.testing.assert_array_equal(got8.astype(np.float64), expect)
+
+
+def test_combine_fp8_against_fp64_within_bound():
+    import torch
+    rng = np.random.default_rng(23)
+    T, H, k, R = 40, 384, 6, 300
+    yq = rng.integers(0, 256, size=(R, H)).astype(np.uint8)
+    yq[(yq & 0x7F) == 0x7F] = 0x11                               # no NaN codes
+    ys = np.exp(rng.uniform(-6, 6, size=(R, H // 128))).astype(np.float32)
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    slot_of = rng.integers(0, R, size=(T, k)).astype(np.int32)
+    slot_of[rng.random((T, k)) < 0.2] = -1
+    out = oracle.combine_fp8(yq, ys, w, slot_of)
+    table = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    vals = table[yq] * np.repeat(ys.astype(np.float64), 128, axis=1)      # [R, H]
+    valid = slot_of >= 0
+    rows = vals[np.where(valid, slot_of, 0)]
+    wv = np.where(valid, w.astype(np.float64), 0.0)[:, :, None]
+    exact = (wv * rows).sum(axis=1)
+    mag = (np.abs(wv) * np.abs(rows)).sum(axis=1)
+    err32 = 3 * k * 2.0 ** -24 * mag                               # dequant, product and sum roundings
+    bound = 2.0 ** -8 * (np.abs(exact) + err32) + err32
+    got = oracle.bf16_to_f32(out).astype(np.float64)
+    assert (np.abs(got - exact) <= bound * (1 + 1e-9) + 1e-300).all()
+    # unweighted = weights of one
+    np.testing.assert_array_equal(oracle.combine_fp8(yq, ys, None, slot_of),
+                                  oracle.combine_fp8(yq, ys, np.ones_like(w), slot_of))
+
+
+def test_fp8_dispatch_then_fp8_combine_returns_x_within_quantisation():
+    d = W.make(W.WORKLOADS["decode"].shrink(16))
+    wl = d["wl"]
+    L = oracle.layout(d["topk_idx"], wl.E, wl.P, oracle.CAPACITY, wl.capacity)
+    q, s, _ = oracle.dispatch_fp8(d["x"], L["slot_of"], wl.R)
+    w = np.full((wl.T, wl.k), 1.0 / wl.k, np.float32)             # exact: k = 8
+    out = oracle.bf16_to_f32(oracle.combine_fp8(q, s, w, L["slot_of"])).astype(np.float64)
+    x = oracle.bf16_to_f32(d["x"]).astype(np.float64)
+    sb = np.repeat(s[L["slot_of"][:, 0]].astype(np.float64), 128, axis=1)
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * sb) * 1.0001 + 2.0 ** -8 * np.abs(x) + 1e-30
+    assert (np.abs(out - x) <= bound).all()

@@ -35,6 +35,9 @@ MUTATIONS = {
     "ue8m0 rounds the scale down": ("float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev);",
                                     "float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev - 1);"),
     "ue8m0 exponent bias": ("uint8_t e8 = (uint8_t)(es - 1 + 127);", "uint8_t e8 = (uint8_t)(es + 127);"),
+    "fp8 combine wrong scale block": ("s = ((const float *)ys)[slot * nb + i / 128];", "s = ((const float *)ys)[slot * nb];"),
+    "fp8 combine ue8m0 bias": ("(int)((const uint8_t *)ys)[slot * nb + i / 128] - 127)",
+                               "(int)((const uint8_t *)ys)[slot * nb + i / 128] - 126)"),
 }
 
 CHECKS = [
@@ -49,6 +52,8 @@ CHECKS = [
     "pf.test_ue8m0_scale_properties_and_codes_match_torch",
     "pf.test_fp8_dispatch_error_bound_and_amax_code",
     "pc.test_golden_combine_example",
+    "pc.test_golden_combine_fp8_example",
+    "pc.test_combine_fp8_against_fp64_within_bound",
     "pc.test_combine_against_fp64_within_bound",
     "pc.test_bf16_rounding_matches_torch",
 ]
@@ -61,7 +66,7 @@ lib_path, checks = sys.argv[1], json.loads(sys.argv[2])
 if lib_path:
     real = oracle._load()
     mutant = ctypes.CDLL(lib_path)
-    for fn in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_dispatch_fp8_ue8m0", "oracle_combine",
+    for fn in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_dispatch_fp8_ue8m0", "oracle_combine", "oracle_combine_fp8",
                "oracle_e4m3_encode_n", "oracle_f32_to_bf16_n", "oracle_e4m3_value"):
         getattr(mutant, fn).restype = getattr(real, fn).restype
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
