@@ -18,9 +18,10 @@ import oracle
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.c")
 
 MUTATIONS = {
-    "combine drops a term": ("acc = acc + prod;", "acc = prod;"),
+    "combine drops a term": ("bf16_bits_to_f32(y[slot * H + i]);\n                acc = acc + prod;",
+                             "bf16_bits_to_f32(y[slot * H + i]);\n                acc = prod;"),
     "combine wrong weight index": ("topk_w[(long)t * k + j] * bf16", "topk_w[(long)t * k] * bf16"),
-    "combine wrong row": ("y[slot * H + i]", "y[(long)t * H + i]"),
+    "combine wrong row": ("bf16_bits_to_f32(y[slot * H + i])", "bf16_bits_to_f32(y[(long)t * H + i])"),
     "layout reversed order in expert": ("slot = offsets[e] + rank;", "slot = offsets[e + 1] - 1 - rank;"),
     "layout walks j before t": ("for (int t = 0; t < T; ++t) {\n        for (int j = 0; j < k; ++j) {\n            long n",
                                 "for (int j = 0; j < k; ++j) {\n        for (int t = 0; t < T; ++t) {\n            long n"),
