@@ -208,6 +208,29 @@ class Plan:
         return out
 
 
+    def combine_fp8(self, y: torch.Tensor, y_scales: torch.Tensor, topk_w: torch.Tensor | None,
+                    stream: torch.cuda.Stream | None = None, out: torch.Tensor | None = None,
+                    slot_of: torch.Tensor | None = None) -> torch.Tensor:
+        """combine() over fp8 expert outputs: y e4m3 [R, H] and y_scales
+        [R, H/128] (float32 scales, or uint8 UE8M0 exponents)."""
+        s = self.shape
+        if tuple(y.shape) != (self.R, s.H) or y.element_size() != 1:
+            raise ValueError(f"y must be one-byte e4m3 [{self.R}, {s.H}]")
+        if tuple(y_scales.shape) != (self.R, s.H // 128):
+            raise ValueError(f"y_scales must be [{self.R}, {s.H // 128}]")
+        if y_scales.dtype not in (torch.float32, torch.uint8):
+            raise TypeError("y_scales must be float32 or uint8 (UE8M0)")
+        payload = PAYLOAD_FP8_E4M3_UE8M0 if y_scales.dtype == torch.uint8 else PAYLOAD_FP8_E4M3
+        out = self.out if out is None else out
+        slot_of = self.layout_out.slot_of if slot_of is None else slot_of
+        st = load().ep_combine_fp8(
+            ctypes.byref(s), _ptr(y, None, "y"), _ptr(y_scales, None, "y_scales"), payload,
+            _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), _ptr(slot_of, torch.int32, "slot_of", s.T * s.k),
+            _ptr(out, torch.bfloat16, "out", s.T * s.H), _ptr(self.layout_out.err_flags), _stream(stream))
+        check(st, "ep_combine_fp8")
+        return out
+
+
 # ------------------------------------------------------- one-shot helpers
 
 def get_layout(topk_idx: torch.Tensor, num_experts: int, num_partitions: int = 1,

@@ -40,7 +40,12 @@ constexpr unsigned kFull = 0xffffffffu;
 __host__ __device__ constexpr uint32_t round128(uint32_t b) { return (b + 127u) / 128u * 128u; }
 __host__ __device__ constexpr uint32_t weights_offset(int ns) { return round128(16u * ns); }
 __host__ __device__ constexpr uint32_t mask_offset(int ns) { return weights_offset(ns) + 128u * ns; }
-__host__ __device__ constexpr uint32_t stages_offset(int ns) { return round128(mask_offset(ns) + 4u * ns); }
+__host__ __device__ constexpr uint32_t scales_offset(int ns) { return round128(mask_offset(ns) + 4u * ns); }
+constexpr int kMaxSliceBlocks = 16;   // fp8: 128-channel blocks per slice at most
+// fp8 expert outputs also stage the block scales of every row: [NS][32][16] f32.
+__host__ __device__ constexpr uint32_t stages_offset(int ns, bool fp8) {
+    return fp8 ? scales_offset(ns) + 32u * kMaxSliceBlocks * 4u * ns : scales_offset(ns);
+}
 constexpr int kConsumerWarps = EP_COMBINE_CONSUMER_WARPS;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kStages = EP_COMBINE_STAGES;
@@ -57,9 +62,43 @@ struct Args {
     int64_t row_bytes;       // H * 2
     int slices;              // units per token row
     int k;
-    uint32_t slice_bytes;    // multiple of 16
+    uint32_t slice_bytes;    // multiple of 16 (bf16) or of 128 (fp8)
     uint32_t stage_bytes;    // k * slice_bytes (rows of one stage are slice_bytes apart)
+    const void* ys;          // fp8 only: scales [R, H/128], f32 or UE8M0 bytes
+    int nb;                  // H / 128
+    int ue8m0;
+    int slice_blocks;        // fp8: 128-channel blocks per slice
 };
+
+// e4m3 code pair (low byte first) -> two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// Value of a UE8M0 exponent byte: 2^(e - 127) (e = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_value(uint32_t e) {
+    return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// Accumulates w * (value(code) * s) for 16 fp8 codes.
+__device__ __forceinline__ void accumulate_fp8(float (&acc)[16], float w, float s, const uint4& v) {
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 a = e4m3x2_to_float2((uint16_t)(words[q] & 0xffffu));
+        const float2 b = e4m3x2_to_float2((uint16_t)(words[q] >> 16));
+        acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], __fmul_rn(w, __fmul_rn(a.x, s)));
+        acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], __fmul_rn(w, __fmul_rn(a.y, s)));
+        acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], __fmul_rn(w, __fmul_rn(b.x, s)));
+        acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], __fmul_rn(w, __fmul_rn(b.y, s)));
+    }
+}
 
 __device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
@@ -74,14 +113,15 @@ __device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4
 // warps 1..kConsumerWarps consume (sum, convert, store) and hand each stage
 // back through its "empty" mbarrier, so index loads and copies of later units
 // overlap the arithmetic of earlier ones.
-template <int NS>
+template <int NS, bool FP8>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                     // [NS] data landed
     uint64_t* empty = full + NS;                                            // [NS] stage free again
     float* w_s = reinterpret_cast<float*>(smem + weights_offset(NS));       // [NS][32] weights, 0 if no row
     uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + mask_offset(NS)); // [NS] valid-row bits
-    unsigned char* stages = smem + stages_offset(NS);
+    float* sc_s = reinterpret_cast<float*>(smem + scales_offset(NS));      // fp8: [NS][32][16] block scales
+    unsigned char* stages = smem + stages_offset(NS, FP8);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -138,6 +178,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
             }
             if (lane < a.k) w_s[s * 32 + lane] = w;
             if (lane == 0) mask_s[s] = valid;
+            if (FP8 && slot >= 0) {
+                const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.slice_blocks;
+                float* dst = sc_s + (s * 32 + lane) * kMaxSliceBlocks;
+                for (int b = 0; b < a.slice_blocks; ++b) {
+                    dst[b] = a.ue8m0 ? ue8m0_value(__ldg(static_cast<const uint8_t*>(a.ys) + s0 + b))
+                                     : __ldg(static_cast<const float*>(a.ys) + s0 + b);
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(valid) * a.slice_bytes);
             __syncwarp();
@@ -172,6 +220,37 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
         if (!ok) break;
         const uint32_t valid = mask_s[s];
         const unsigned char* st = stages + (size_t)s * a.stage_bytes;
+        if (FP8) {
+            // 16 channels per step: 16 code bytes in, 32 bf16 bytes out
+            unsigned char* dst = a.out + (t * a.row_bytes + (int64_t)sl * a.slice_bytes) * 2;
+            for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
+                const int blk = (ch * 16) / 128;
+                float acc[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+                for (int j = 0; j < a.k; ++j) {
+                    if (valid & (1u << j)) {
+                        const uint4 v =
+                            *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
+                        accumulate_fp8(acc, w_s[s * 32 + j], sc_s[(s * 32 + j) * kMaxSliceBlocks + blk], v);
+                    }
+                }
+                uint4 o0, o1;
+                o0.x = pack_bf16x2(acc[0], acc[1]);
+                o0.y = pack_bf16x2(acc[2], acc[3]);
+                o0.z = pack_bf16x2(acc[4], acc[5]);
+                o0.w = pack_bf16x2(acc[6], acc[7]);
+                o1.x = pack_bf16x2(acc[8], acc[9]);
+                o1.y = pack_bf16x2(acc[10], acc[11]);
+                o1.z = pack_bf16x2(acc[12], acc[13]);
+                o1.w = pack_bf16x2(acc[14], acc[15]);
+                *reinterpret_cast<uint4*>(dst + ch * 32) = o0;
+                *reinterpret_cast<uint4*>(dst + ch * 32 + 16) = o1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            continue;
+        }
         unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
         for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
             float acc[8];
@@ -212,6 +291,34 @@ int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t 
     return best ? best : (int)n;
 }
 
+
+template <bool FP8>
+cudaError_t launch_ring(Args& a, int num_sms, cudaStream_t stream) {
+    // If one single-stage CTA per unit fits on the GPU at once (small
+    // batches), launch exactly that: every unit starts immediately.  Otherwise
+    // a persistent grid of kStages-deep rings.
+    auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
+        smem = stages_offset(ns, FP8) + (size_t)ns * a.stage_bytes;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
+        return e;
+    };
+    size_t smem = 0;
+    int64_t ctas = 0;
+    cudaError_t err = resident(combine_kernel<1, FP8>, 1, smem, ctas);
+    if (err != cudaSuccess) return err;
+    if (a.units <= ctas) {
+        return launch_kernel(true, combine_kernel<1, FP8>, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
+    }
+    err = resident(combine_kernel<kStages, FP8>, kStages, smem, ctas);
+    if (err != cudaSuccess) return err;
+    const int64_t grid = ctas < a.units ? ctas : a.units;
+    return launch_kernel(false, combine_kernel<kStages, FP8>, dim3((unsigned)grid), dim3(kThreads), smem, stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t stream) {
@@ -224,38 +331,30 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
     a.err_flags = p.err_flags;
     a.R = p.R;
     a.k = p.k;
-    a.row_bytes = (int64_t)p.H * 2;
-    // A stage holds k slices; slices of at most kStageBytesMax / k bytes, at
-    // least 256 bytes once one size fits, enough units for ~4 per SM.
-    const int64_t vec16 = a.row_bytes / 16;
-    const int64_t max_per = (int64_t)(kStageBytesMax / 16) / p.k;
-    a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, 4LL * num_sms);
-    a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+    a.nb = p.H / 128;
+    if (p.fp8) {
+        // Slices of whole 128-channel blocks (their scales are staged too), at
+        // most kStageBytesMax / k bytes and kMaxSliceBlocks blocks.
+        a.ys = p.y_scales;
+        a.ue8m0 = p.ue8m0;
+        a.row_bytes = p.H;
+        int64_t max_blocks = (int64_t)(kStageBytesMax / 128) / p.k;
+        if (max_blocks > kMaxSliceBlocks) max_blocks = kMaxSliceBlocks;
+        a.slices = pick_slices(p.T, a.nb, max_blocks > 0 ? max_blocks : 1, 1, 4LL * num_sms);
+        a.slice_blocks = a.nb / a.slices;
+        a.slice_bytes = (uint32_t)a.slice_blocks * 128u;
+    } else {
+        // A stage holds k slices; slices of at most kStageBytesMax / k bytes,
+        // at least 256 bytes once one size fits, enough units for ~4 per SM.
+        a.row_bytes = (int64_t)p.H * 2;
+        const int64_t vec16 = a.row_bytes / 16;
+        const int64_t max_per = (int64_t)(kStageBytesMax / 16) / p.k;
+        a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, 4LL * num_sms);
+        a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+    }
     a.stage_bytes = a.slice_bytes * (uint32_t)p.k;
     a.units = (int64_t)p.T * a.slices;
-    // If one single-stage CTA per unit fits on the GPU at once (small
-    // batches), launch exactly that: every unit starts immediately.  Otherwise
-    // a persistent grid of kStages-deep rings.
-    auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
-        smem = stages_offset(ns) + (size_t)ns * a.stage_bytes;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
-        return e;
-    };
-    size_t smem = 0;
-    int64_t ctas = 0;
-    cudaError_t err = resident(combine_kernel<1>, 1, smem, ctas);
-    if (err != cudaSuccess) return err;
-    if (a.units <= ctas) {
-        return launch_kernel(true, combine_kernel<1>, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
-    }
-    err = resident(combine_kernel<kStages>, kStages, smem, ctas);
-    if (err != cudaSuccess) return err;
-    const int64_t grid = ctas < a.units ? ctas : a.units;
-    return launch_kernel(false, combine_kernel<kStages>, dim3((unsigned)grid), dim3(kThreads), smem, stream, a);
+    return p.fp8 ? launch_ring<true>(a, num_sms, stream) : launch_ring<false>(a, num_sms, stream);
 }
 
 }  // namespace ep

@@ -275,4 +275,39 @@ ep_status_t ep_combine(const ep_shape_t* shape, const void* y, const float* topk
     return launched(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)), "combine launch");
 }
 
+ep_status_t ep_combine_fp8(const ep_shape_t* shape, const void* y, const void* y_scales, int32_t payload,
+                           const float* topk_w, const int32_t* slot_of, void* out, uint32_t* err_flags,
+                           ep_stream_t stream) {
+    ep_status_t st = check_shape(shape);
+    if (st != EP_OK) return st;
+    if (payload != EP_PAYLOAD_FP8_E4M3 && payload != EP_PAYLOAD_FP8_E4M3_UE8M0)
+        return fail(EP_ERR_INVALID_ARG, "payload = %d is not an fp8 payload format", payload);
+    if (shape->H % 128 != 0) return fail(EP_ERR_INVALID_ARG, "fp8 expert outputs need H %% 128 == 0 (H = %d)", shape->H);
+    if (shape->T == 0) return ok();
+    const bool ue8m0 = payload == EP_PAYLOAD_FP8_E4M3_UE8M0;
+    if (y == nullptr || y_scales == nullptr || slot_of == nullptr || out == nullptr)
+        return fail(EP_ERR_INVALID_ARG, "y / y_scales / slot_of / out is NULL");
+    if (!aligned16(y) || !aligned16(out)) return fail(EP_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
+    if (!ue8m0 && (reinterpret_cast<uintptr_t>(y_scales) & 3u))
+        return fail(EP_ERR_INVALID_ARG, "f32 y_scales must be 4-byte aligned");
+    int num_sms = 0;
+    st = device_info(&num_sms);
+    if (st != EP_OK) return st;
+
+    ep::CombineParams p{};
+    p.y = y;
+    p.y_scales = y_scales;
+    p.fp8 = 1;
+    p.ue8m0 = ue8m0 ? 1 : 0;
+    p.topk_w = topk_w;
+    p.slot_of = slot_of;
+    p.out = out;
+    p.err_flags = err_flags;
+    p.R = rows_of(shape);
+    p.T = shape->T;
+    p.H = shape->H;
+    p.k = shape->k;
+    return launched(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)), "combine launch");
+}
+
 }  // extern "C"

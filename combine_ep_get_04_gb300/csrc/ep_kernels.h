@@ -110,7 +110,9 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
 // ---------------------------------------------------------------- combine
 
 struct CombineParams {
-    const void* y;          // bf16 [R, H]
+    const void* y;          // bf16 [R, H], or e4m3 [R, H] with fp8
+    const void* y_scales;   // fp8: [R, H/128] f32, or u8 exponents with ue8m0
+    int fp8, ue8m0;
     const float* topk_w;    // [T, k]
     const int32_t* slot_of; // [T, k]
     void* out;              // bf16 [T, H]

@@ -247,6 +247,26 @@ EP_API ep_status_t ep_combine(const ep_shape_t *shape, const void *y,
                        const float *topk_w, const int32_t *slot_of, void *out,
                        uint32_t *err_flags, ep_stream_t stream);
 
+/*
+ * ep_combine_fp8 -- ep_combine over fp8 expert outputs (the e4m3 variant of
+ * the combine the pages measure beside dispatch, "Pipeline direct NVLink
+ * dispatch with triple-buffered prefetch", Validation table).
+ *
+ * In:  y        e4m3 [R, H] expert outputs in the receive layout, 16-byte
+ *               aligned; H % 128 == 0.
+ *      y_scales payload EP_PAYLOAD_FP8_E4M3: f32 [R, H/128] (4-byte aligned);
+ *               EP_PAYLOAD_FP8_E4M3_UE8M0: u8 [R, H/128] biased exponents,
+ *               scale = 2^(e - 127).
+ *      topk_w, slot_of, out, err_flags as ep_combine.
+ * Each element is dequantised as v = value(code) * scale (fp32 product,
+ * rounded to nearest), then out[t] = bf16( sum_j topk_w[t,j] * v ) in fp32 in
+ * increasing j, as ep_combine.
+ */
+EP_API ep_status_t ep_combine_fp8(const ep_shape_t *shape, const void *y,
+                       const void *y_scales, int32_t payload,
+                       const float *topk_w, const int32_t *slot_of, void *out,
+                       uint32_t *err_flags, ep_stream_t stream);
+
 /* Static description of a status code. */
 EP_API const char *ep_status_string(ep_status_t status);
 

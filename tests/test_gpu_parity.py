@@ -508,3 +508,50 @@ def test_expert_side_weights_round_trip():
     a = plan.combine(y_weighted, None).float().clone()
     b = plan.combine(recv, dev(d["topk_w"])).float()
     assert bool(((a - b).abs() <= ATOL + RTOL * b.abs()).all())
+
+
+# ------------------------------------------------- combine of fp8 expert outputs
+
+def _fp8_expert_outputs(rng, R, H, ue8m0):
+    q = rng.integers(0, 256, size=(R, H)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3A                                   # no NaN codes
+    if ue8m0:
+        s = rng.integers(100, 140, size=(R, H // 128)).astype(np.uint8)
+    else:
+        s = np.exp(rng.uniform(-8, 8, size=(R, H // 128))).astype(np.float32)
+    return q, s
+
+
+@pytest.mark.parametrize("T,H,E,k,cap,ue8m0,weighted", [
+    (128, 7168, 256, 8, 128, False, True), (128, 7168, 256, 8, 128, True, True), (1, 128, 4, 1, None, False, True),
+    (9, 384, 8, 3, None, True, False), (200, 1024, 16, 8, None, False, True), (5, 65536, 4, 2, None, True, True),
+    (640, 7168, 256, 8, None, False, True)])
+def test_combine_fp8_matches_oracle(T, H, E, k, cap, ue8m0, weighted):
+    rng = np.random.default_rng(T + H + 31 * ue8m0)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[rng.random((T, k)) < 0.05] = -1
+    wl = W.Workload("c8", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=True,
+                    mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
+    q, s = _fp8_expert_outputs(rng, wl.R, H, ue8m0)
+    w = rng.standard_normal((T, k)).astype(np.float32) if weighted else None
+    plan = plan_for(wl)
+    plan.layout(dev(idx))
+    out = plan.combine_fp8(dev(q).view(torch.float8_e4m3fn), dev(s), None if w is None else dev(w))
+    torch.cuda.synchronize()
+    L = oracle_layout(wl, idx)
+    assert_combine_close(bits(out), oracle.combine_fp8(q, s, w, L["slot_of"]))
+
+
+def test_fp8_dispatch_then_fp8_combine_round_trip_decode():
+    """GPU fp8 dispatch into the capacity buffer, identity experts, GPU fp8 combine ~ x."""
+    d = W.make("decode")
+    wl = d["wl"]
+    plan = plan_for(wl)
+    x = bf16_dev(d["x"])
+    L, q, s, _ = plan.layout_dispatch(dev(d["topk_idx"]), x)
+    w = torch.full((wl.T, wl.k), 1.0 / wl.k, device="cuda")
+    out = plan.combine_fp8(q, s, w).float()
+    xf = x.float()
+    sb = s[L.slot_of[:, 0].long()].repeat_interleave(128, dim=1)
+    bound = torch.maximum(2.0 ** -4 * xf.abs(), 2.0 ** -10 * sb) * 1.0001 + 2.0 ** -8 * xf.abs() + 1e-30
+    assert bool(((out - xf).abs() <= bound).all())
