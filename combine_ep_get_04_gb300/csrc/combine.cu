@@ -24,6 +24,9 @@
 #ifndef EP_COMBINE_STAGE_BYTES
 #define EP_COMBINE_STAGE_BYTES 16384
 #endif
+#ifndef EP_COMBINE_UNITS_PER_SM
+#define EP_COMBINE_UNITS_PER_SM 4     // units the slice size aims at, per SM
+#endif
 #ifndef EP_COMBINE_CONSUMER_WARPS
 #define EP_COMBINE_CONSUMER_WARPS 4
 #endif
@@ -340,7 +343,7 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
         a.row_bytes = p.H;
         int64_t max_blocks = (int64_t)(kStageBytesMax / 128) / p.k;
         if (max_blocks > kMaxSliceBlocks) max_blocks = kMaxSliceBlocks;
-        a.slices = pick_slices(p.T, a.nb, max_blocks > 0 ? max_blocks : 1, 1, 4LL * num_sms);
+        a.slices = pick_slices(p.T, a.nb, max_blocks > 0 ? max_blocks : 1, 1, (int64_t)EP_COMBINE_UNITS_PER_SM * num_sms);
         a.slice_blocks = a.nb / a.slices;
         a.slice_bytes = (uint32_t)a.slice_blocks * 128u;
     } else {
@@ -349,7 +352,7 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
         a.row_bytes = (int64_t)p.H * 2;
         const int64_t vec16 = a.row_bytes / 16;
         const int64_t max_per = (int64_t)(kStageBytesMax / 16) / p.k;
-        a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, 4LL * num_sms);
+        a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, (int64_t)EP_COMBINE_UNITS_PER_SM * num_sms);
         a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
     }
     a.stage_bytes = a.slice_bytes * (uint32_t)p.k;

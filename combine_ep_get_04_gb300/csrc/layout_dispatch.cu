@@ -20,6 +20,11 @@
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
+// Units (CTAs) per SM the slice size aims at (compile-time; tuned value).
+#ifndef EP_FUSED_UNITS_PER_SM
+#define EP_FUSED_UNITS_PER_SM 1
+#endif
+
 namespace ep {
 
 namespace {
@@ -376,13 +381,13 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
     a.ue8m0 = f.ue8m0;
     if (f.fp8) {
         a.nb = f.H / 128;
-        a.slices = pick_divisor(f.T, a.nb, 64, 2, (int64_t)num_sms);
+        a.slices = pick_divisor(f.T, a.nb, 64, 2, (int64_t)EP_FUSED_UNITS_PER_SM * num_sms);
         a.nblk = a.nb / a.slices;
         a.scale_bulk = (a.nb % 4 == 0) && (a.nblk % 4 == 0);
         a.in_bytes = (uint32_t)a.nblk * 256u;
     } else {
         const int64_t vec16 = (int64_t)f.H * 2 / 16;
-        a.slices = pick_divisor(f.T, vec16, 1024, 64, (int64_t)num_sms);
+        a.slices = pick_divisor(f.T, vec16, 1024, 64, (int64_t)EP_FUSED_UNITS_PER_SM * num_sms);
         a.in_bytes = (uint32_t)(vec16 / a.slices * 16);
     }
     a.in_stride = (a.in_bytes + 127u) & ~127u;
