@@ -19,6 +19,10 @@ Functions and the passages they follow (DeepEP web pages):
   combine       -- weighted top-k reduce back to token order, fp32
                    accumulation, bf16 result (same PR, Validation table);
                    also over fp8 expert outputs with per-128-channel scales.
+  combine_src   -- the same reduce with each copy found through the
+                   expert-side record of where it came from (src_token,
+                   src_k) and a per-row weight carried with the row (same
+                   PR, Summary: routing information travels with the token).
 All of them are pinned (tests/test_oracle_*.py); none is "parity unpinned".
 """
 from __future__ import annotations
@@ -74,6 +78,8 @@ def _load():
             lib.oracle_combine_fp8.restype = None
             lib.oracle_combine_fp8.argtypes = [ctypes.c_int] * 3 + [vp, vp, ctypes.c_int, vp, vp, vp]
             lib.oracle_combine.restype = None
+            lib.oracle_combine_src.restype = None
+            lib.oracle_combine_src.argtypes = [ctypes.c_int] * 3 + [ctypes.c_long] + [vp] * 5
             lib.oracle_combine.argtypes = [ctypes.c_int] * 3 + [vp] * 4
             lib.oracle_e4m3_encode_n.restype = None
             lib.oracle_e4m3_encode_n.argtypes = [vp, vp, ctypes.c_long]
@@ -206,6 +212,25 @@ def combine_fp8(yq: np.ndarray, ys: np.ndarray, topk_w: np.ndarray | None, slot_
     w = None if topk_w is None else np.ascontiguousarray(topk_w, dtype=np.float32)
     out = np.zeros((T, H), np.uint16)
     _load().oracle_combine_fp8(T, H, k, _ptr(yq), _ptr(ys), int(ue8m0), _ptr(w), _ptr(slot_of), _ptr(out))
+    return out
+
+
+def combine_src(y: np.ndarray, row_w: np.ndarray | None, src_token: np.ndarray, src_k: np.ndarray,
+                T: int, k: int) -> np.ndarray:
+    """Combine addressed by the expert-side maps: y [R, H] uint16 (bf16 bits),
+    row_w [R] float32 or None (unit weights), src_token / src_k [R] int32
+    (-1 in rows without a copy); returns out [T, H] uint16 (bf16 bits)."""
+    if k > 64:
+        raise ValueError("combine_src takes k <= 64")
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    R, H = y.shape
+    src_token = np.ascontiguousarray(src_token, dtype=np.int32)
+    src_k = np.ascontiguousarray(src_k, dtype=np.int32)
+    if src_token.shape != (R,) or src_k.shape != (R,):
+        raise ValueError("src_token and src_k need one entry per row of y")
+    w = None if row_w is None else np.ascontiguousarray(row_w, dtype=np.float32)
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine_src(T, H, k, R, _ptr(y), _ptr(w), _ptr(src_token), _ptr(src_k), _ptr(out))
     return out
 
 

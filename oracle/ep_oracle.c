@@ -406,6 +406,44 @@ void oracle_combine_fp8(int T, int H, int k, const uint8_t *y, const void *ys, i
     }
 }
 
+/*
+ * combine addressed from the expert side.  Row r of the expert-major buffer
+ * y [R, H] carries the pair it was dispatched from, (src_token[r], src_k[r]),
+ * or -1 when it holds no copy, and optionally its own weight row_w[r] (NULL:
+ * every weight is 1).  Copy j of token t is the row whose pair is (t, j),
+ * found by scanning the rows from 0 up (the first such row if several claim
+ * it); a pair that no row holds (a dropped or masked copy) adds nothing.
+ * out[t, i] = bf16( sum over j of w_r * y[r, i] ), fp32 in increasing j,
+ * exactly as oracle_combine does with slot_of[t,j] = r.
+ */
+void oracle_combine_src(int T, int H, int k, long R, const uint16_t *y, const float *row_w,
+                        const int32_t *src_token, const int32_t *src_k, uint16_t *out)
+{
+    long row_of_copy[64];
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            row_of_copy[j] = -1;
+            for (long r = 0; r < R; ++r) {
+                if (src_token[r] == t && src_k[r] == j) {
+                    row_of_copy[j] = r;
+                    break;
+                }
+            }
+        }
+        for (int i = 0; i < H; ++i) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                long r = row_of_copy[j];
+                if (r < 0) continue;
+                float w = row_w ? row_w[r] : 1.0f;
+                float prod = w * bf16_bits_to_f32(y[r * H + i]);
+                acc = acc + prod;
+            }
+            out[(long)t * H + i] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
 /* Vector helpers for the tests (elementwise over n values). */
 void oracle_e4m3_encode_n(const float *v, uint8_t *codes, long n)
 {

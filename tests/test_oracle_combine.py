@@ -4,7 +4,10 @@ Pinned against: the hand-worked example in golden/combine_example.txt; an
 fp64 recomputation with numpy inside the error bound derived from the
 arithmetic (fp32 products and sums, one bf16 rounding); identity experts with
 weights whose partial sums are exact (result must equal x bit for bit); and
-the bit-copy invariant of bf16 dispatch.
+the bit-copy invariant of bf16 dispatch.  The combine addressed through the
+expert-side source maps is pinned by its own hand-worked example (packed,
+unweighted and capacity maps), the fp64 bound with the inverse map rebuilt in
+numpy, and bit equality with the slot_of combine on oracle layouts.
 """
 import numpy as np
 import torch
@@ -181,3 +184,72 @@ def test_fp8_dispatch_then_fp8_combine_returns_x_within_quantisation():
     sb = np.repeat(s[L["slot_of"][:, 0]].astype(np.float64), 128, axis=1)
     bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * sb) * 1.0001 + 2.0 ** -8 * np.abs(x) + 1e-30
     assert (np.abs(out - x) <= bound).all()
+
+
+# ---- combine addressed from the expert side (src_token / src_k, per-row weights)
+
+def test_golden_combine_src_example():
+    g = read_golden_kv("combine_src_example.txt")
+    H, T, k = (int(g[n][0]) for n in ("H", "T", "k"))
+    y = W.to_bf16_bits(floats(g["y"]).reshape(-1, H).astype(np.float32))
+    for prefix, wkey, outkey in (("", "row_w", "out"), ("", None, "out_unweighted"), ("cap_", "cap_row_w", "cap_out")):
+        st = ints(g[prefix + "src_token"]).astype(np.int32)
+        sk = ints(g[prefix + "src_k"]).astype(np.int32)
+        rw = None if wkey is None else floats(g[wkey]).astype(np.float32)
+        out = oracle.combine_src(y, rw, st, sk, T, k)
+        np.testing.assert_array_equal(oracle.bf16_to_f32(out).ravel(), floats(g[outkey]).astype(np.float32),
+                                      err_msg=outkey)
+
+
+def _inverse_maps(src_token, src_k, T, k):
+    """slot[t, j] = the row holding (t, j), -1 if none (numpy, independent of the C code)."""
+    slot = np.full((T, k), -1, np.int32)
+    live = np.nonzero(src_token >= 0)[0]
+    slot[src_token[live], src_k[live]] = live
+    return slot
+
+
+def test_combine_src_against_fp64_within_bound():
+    rng = np.random.default_rng(21)
+    for T, H, k, R, drop in [(40, 48, 8, 500, 0.2), (9, 8, 1, 12, 0.0), (25, 16, 5, 200, 0.5)]:
+        # a random injective placement of the live (t, j) pairs into R rows
+        pairs = [(t, j) for t in range(T) for j in range(k) if rng.random() >= drop]
+        rows = rng.permutation(R)[: len(pairs)]
+        src_token = np.full(R, -1, np.int32)
+        src_k = np.full(R, -1, np.int32)
+        for (t, j), r in zip(pairs, rows):
+            src_token[r], src_k[r] = t, j
+        y = W.to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32) * 2)
+        row_w = rng.standard_normal(R).astype(np.float32)
+        out = oracle.combine_src(y, row_w, src_token, src_k, T, k)
+        slot = _inverse_maps(src_token, src_k, T, k)
+        w = np.where(slot >= 0, row_w[np.maximum(slot, 0)], 0).astype(np.float32)
+        _fp64_bound_check(y, w, slot, out)
+
+
+def test_combine_src_equals_slot_combine_on_layouts():
+    """Rows found through the expert-side maps give exactly the slot_of combine
+    (same products, same j order), packed and capacity, with masked copies."""
+    rng = np.random.default_rng(8)
+    for T, E, k, P, cap, mask in [(100, 16, 4, 4, None, 0.1), (64, 8, 8, 2, 40, 0.0), (30, 32, 3, 8, 2, 0.2)]:
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+        idx[rng.random((T, k)) < mask] = -1
+        if cap is None:
+            L = oracle.layout(idx, E, P)
+            R = T * k
+        else:
+            L = oracle.layout(idx, E, P, mode=oracle.CAPACITY, cap=cap)
+            R = E * cap
+        H = 24
+        y = W.to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+        topk_w = rng.random((T, k)).astype(np.float32)
+        st, sk = L["src_token"], L["src_k"]
+        row_w = np.where(st >= 0, topk_w[np.maximum(st, 0), np.maximum(sk, 0)], 7.0).astype(np.float32)
+        np.testing.assert_array_equal(oracle.combine_src(y, row_w, st, sk, T, k),
+                                      oracle.combine(y, topk_w, L["slot_of"]))
+        np.testing.assert_array_equal(oracle.combine_src(y, None, st, sk, T, k),
+                                      oracle.combine(y, np.ones((T, k), np.float32), L["slot_of"]))
+        # the row order of the expert-side buffer does not matter
+        p = rng.permutation(R)
+        np.testing.assert_array_equal(oracle.combine_src(y[p], row_w[p], st[p], sk[p], T, k),
+                                      oracle.combine(y, topk_w, L["slot_of"]))

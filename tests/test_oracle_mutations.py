@@ -37,6 +37,9 @@ MUTATIONS = {
                                     "float s = (mant == 0.5f) ? v : ldexpf(1.0f, ev - 1);"),
     "ue8m0 exponent bias": ("uint8_t e8 = (uint8_t)(es - 1 + 127);", "uint8_t e8 = (uint8_t)(es + 127);"),
     "fp8 combine wrong scale block": ("s = ((const float *)ys)[slot * nb + i / 128];", "s = ((const float *)ys)[slot * nb];"),
+    "combine_src ignores the top-k position": ("if (src_token[r] == t && src_k[r] == j) {",
+                                               "if (src_token[r] == t) {"),
+    "combine_src ignores the row weight": ("float w = row_w ? row_w[r] : 1.0f;", "float w = 1.0f;"),
     "fp8 combine ue8m0 bias": ("(int)((const uint8_t *)ys)[slot * nb + i / 128] - 127)",
                                "(int)((const uint8_t *)ys)[slot * nb + i / 128] - 126)"),
 }
@@ -54,6 +57,7 @@ CHECKS = [
     "pf.test_fp8_dispatch_error_bound_and_amax_code",
     "pc.test_golden_combine_example",
     "pc.test_golden_combine_fp8_example",
+    "pc.test_golden_combine_src_example",
     "pc.test_combine_fp8_against_fp64_within_bound",
     "pc.test_combine_against_fp64_within_bound",
     "pc.test_bf16_rounding_matches_torch",
