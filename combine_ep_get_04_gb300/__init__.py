@@ -119,6 +119,8 @@ class Plan:
         ws = layout_workspace_bytes(self.shape)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.workspace_bytes = ws
+        self.src_workspace_bytes = int(load().ep_combine_src_workspace_bytes(ctypes.byref(self.shape)))
+        self.src_workspace = torch.empty(max(self.src_workspace_bytes, 1), dtype=torch.uint8, device=dev)
         self.layout_out = Layout(
             counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
             part_counts=torch.empty(num_partitions, **i32), part_offsets=torch.empty(num_partitions + 1, **i32),
@@ -228,6 +230,39 @@ class Plan:
             _ptr(topk_w, torch.float32, "topk_w", s.T * s.k), _ptr(slot_of, torch.int32, "slot_of", s.T * s.k),
             _ptr(out, torch.bfloat16, "out", s.T * s.H), _ptr(self.layout_out.err_flags), _stream(stream))
         check(st, "ep_combine_fp8")
+        return out
+
+
+    def combine_src(self, y: torch.Tensor, row_w: torch.Tensor | None, src_token: torch.Tensor | None = None,
+                    src_k: torch.Tensor | None = None, y_scales: torch.Tensor | None = None,
+                    stream: torch.cuda.Stream | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+        """combine() addressed from the expert side: each row r of y is found
+        through the pair (src_token[r], src_k[r]) it holds and weighted by
+        row_w[r] (None: unweighted).  y is bf16 [R, H], or e4m3 [R, H] with
+        y_scales [R, H/128] (float32, or uint8 UE8M0).  The maps default to
+        this plan's last layout."""
+        s = self.shape
+        if tuple(y.shape) != (self.R, s.H):
+            raise ValueError(f"y must be [{self.R}, {s.H}], got {tuple(y.shape)}")
+        if y_scales is None:
+            payload, ys = PAYLOAD_BF16, None
+            yp = _ptr(y, torch.bfloat16, "y")
+        else:
+            if y.element_size() != 1 or tuple(y_scales.shape) != (self.R, s.H // 128):
+                raise ValueError(f"fp8 y must be one-byte [{self.R}, {s.H}] with y_scales [{self.R}, {s.H // 128}]")
+            if y_scales.dtype not in (torch.float32, torch.uint8):
+                raise TypeError("y_scales must be float32 or uint8 (UE8M0)")
+            payload = PAYLOAD_FP8_E4M3_UE8M0 if y_scales.dtype == torch.uint8 else PAYLOAD_FP8_E4M3
+            yp, ys = _ptr(y, None, "y"), _ptr(y_scales, None, "y_scales")
+        src_token = self.layout_out.src_token if src_token is None else src_token
+        src_k = self.layout_out.src_k if src_k is None else src_k
+        out = self.out if out is None else out
+        st = load().ep_combine_src(
+            ctypes.byref(s), yp, ys, payload, _ptr(row_w, torch.float32, "row_w", self.R),
+            _ptr(src_token, torch.int32, "src_token", self.R), _ptr(src_k, torch.int32, "src_k", self.R),
+            _ptr(out, torch.bfloat16, "out", s.T * s.H), _ptr(self.src_workspace), self.src_workspace_bytes,
+            _ptr(self.layout_out.err_flags), _stream(stream))
+        check(st, "ep_combine_src")
         return out
 
 

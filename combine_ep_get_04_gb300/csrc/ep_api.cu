@@ -81,7 +81,7 @@ void record_last_error(const char* msg) { g_last_error = msg; }
 
 extern "C" {
 
-int32_t ep_abi_version(void) { return 100; }
+int32_t ep_abi_version(void) { return 101; }
 
 const char* ep_status_string(ep_status_t st) {
     switch (st) {
@@ -308,6 +308,58 @@ ep_status_t ep_combine_fp8(const ep_shape_t* shape, const void* y, const void* y
     p.H = shape->H;
     p.k = shape->k;
     return launched(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)), "combine launch");
+}
+
+size_t ep_combine_src_workspace_bytes(const ep_shape_t* shape) {
+    if (check_shape(shape) != EP_OK) return 0;
+    return ep::combine_src_workspace_bytes(shape->T, shape->k);
+}
+
+ep_status_t ep_combine_src(const ep_shape_t* shape, const void* y, const void* y_scales, int32_t payload,
+                           const float* row_w, const int32_t* src_token, const int32_t* src_k, void* out,
+                           void* workspace, size_t workspace_bytes, uint32_t* err_flags, ep_stream_t stream) {
+    ep_status_t st = check_shape(shape);
+    if (st != EP_OK) return st;
+    if (payload != EP_PAYLOAD_BF16 && payload != EP_PAYLOAD_FP8_E4M3 && payload != EP_PAYLOAD_FP8_E4M3_UE8M0)
+        return fail(EP_ERR_INVALID_ARG, "payload = %d is not a payload format", payload);
+    const bool fp8 = payload != EP_PAYLOAD_BF16;
+    const bool ue8m0 = payload == EP_PAYLOAD_FP8_E4M3_UE8M0;
+    if (fp8 && shape->H % 128 != 0)
+        return fail(EP_ERR_INVALID_ARG, "fp8 expert outputs need H %% 128 == 0 (H = %d)", shape->H);
+    if (shape->T == 0) return ok();
+    if (y == nullptr || out == nullptr || workspace == nullptr)
+        return fail(EP_ERR_INVALID_ARG, "y / out / workspace is NULL");
+    const int64_t R = rows_of(shape);
+    if (R > 0 && (src_token == nullptr || src_k == nullptr))
+        return fail(EP_ERR_INVALID_ARG, "src_token / src_k is NULL");
+    if (fp8 && y_scales == nullptr) return fail(EP_ERR_INVALID_ARG, "fp8 expert outputs need y_scales");
+    if (!aligned16(y) || !aligned16(out)) return fail(EP_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
+    if (fp8 && !ue8m0 && (reinterpret_cast<uintptr_t>(y_scales) & 3u))
+        return fail(EP_ERR_INVALID_ARG, "f32 y_scales must be 4-byte aligned");
+    const size_t need = ep::combine_src_workspace_bytes(shape->T, shape->k);
+    if (workspace_bytes < need)
+        return fail(EP_ERR_INVALID_ARG, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 3u) return fail(EP_ERR_INVALID_ARG, "workspace is not 4-byte aligned");
+    int num_sms = 0;
+    st = device_info(&num_sms);
+    if (st != EP_OK) return st;
+
+    ep::CombineSrcParams p{};
+    p.base.y = y;
+    p.base.y_scales = fp8 ? y_scales : nullptr;
+    p.base.fp8 = fp8 ? 1 : 0;
+    p.base.ue8m0 = ue8m0 ? 1 : 0;
+    p.base.out = out;
+    p.base.err_flags = err_flags;
+    p.base.R = R;
+    p.base.T = shape->T;
+    p.base.H = shape->H;
+    p.base.k = shape->k;
+    p.row_w = row_w;
+    p.src_token = src_token;
+    p.src_k = src_k;
+    p.workspace = workspace;
+    return launched(ep::launch_combine_src(p, num_sms, reinterpret_cast<cudaStream_t>(stream)), "combine_src launch");
 }
 
 }  // extern "C"

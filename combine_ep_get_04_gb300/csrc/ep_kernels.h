@@ -123,4 +123,20 @@ struct CombineParams {
 
 cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t stream);
 
+// The combine addressed by the expert-side maps: base carries y, scales,
+// out, err_flags and the shape (its slot_of / topk_w are ignored).
+struct CombineSrcParams {
+    CombineParams base;
+    const float* row_w;       // [R] or nullptr (unweighted)
+    const int32_t* src_token; // [R], -1 = no copy
+    const int32_t* src_k;     // [R]
+    void* workspace;          // combine_src_workspace_bytes(T, k) bytes
+};
+
+// Bytes of one [T, k] map rounded up to 256; the workspace holds two.
+size_t combine_src_map_bytes(int64_t T, int k);
+inline size_t combine_src_workspace_bytes(int64_t T, int k) { return 2 * combine_src_map_bytes(T, k); }
+
+cudaError_t launch_combine_src(const CombineSrcParams& p, int num_sms, cudaStream_t stream);
+
 }  // namespace ep

@@ -267,6 +267,42 @@ EP_API ep_status_t ep_combine_fp8(const ep_shape_t *shape, const void *y,
                        const float *topk_w, const int32_t *slot_of, void *out,
                        uint32_t *err_flags, ep_stream_t stream);
 
+/*
+ * ep_combine_src -- the combine addressed from the expert side.  The caller
+ * holds, for every row of the expert-major buffer, the token and top-k
+ * position the row was dispatched from (ep_get_layout's src_token / src_k)
+ * and, optionally, the row's own weight (ep_dispatch's recv_w: the routing
+ * information that travels with each token, "Pipeline direct NVLink dispatch
+ * with triple-buffered prefetch", Summary), instead of the token-side slot_of.
+ * Copy j of token t is the row r with (src_token[r], src_k[r]) = (t, j); the
+ * rows are read in place (no copy of y is made).
+ *
+ * In:  y, y_scales, payload  as ep_combine (payload EP_PAYLOAD_BF16, y_scales
+ *               NULL) or ep_combine_fp8 (the two fp8 payloads).
+ *      row_w    f32 [R] weight of each row, or NULL for an unweighted sum.
+ *      src_token, src_k  i32 [R]: the pair each row holds, src_token = -1 in a
+ *               row that holds no copy.  Each pair appears in at most one row
+ *               (as ep_get_layout writes them; if several rows claim a pair,
+ *               which one is used is unspecified).  A row whose pair lies
+ *               outside [0,T) x [0,k) (other than src_token = -1) is skipped
+ *               and flags EP_ERRF_BAD_SLOT.
+ *      workspace  device memory of ep_combine_src_workspace_bytes(shape)
+ *               bytes, 4-byte aligned, caller-owned; its contents on entry do
+ *               not matter.  It receives the token-side map rebuilt from the
+ *               source maps, [T, k] rows then [T, k] weights.
+ * Out: out      bf16 [T, H]: exactly what ep_combine / ep_combine_fp8 give
+ *               with slot_of[t,j] = r and topk_w[t,j] = row_w[r] (bit for
+ *               bit): fp32 sum in increasing j, one rounding to bf16; a pair
+ *               that no row holds (a dropped or masked copy) adds nothing.
+ * err_flags: EP_ERRF_BAD_SLOT.
+ */
+EP_API size_t ep_combine_src_workspace_bytes(const ep_shape_t *shape);
+EP_API ep_status_t ep_combine_src(const ep_shape_t *shape, const void *y,
+                       const void *y_scales, int32_t payload, const float *row_w,
+                       const int32_t *src_token, const int32_t *src_k, void *out,
+                       void *workspace, size_t workspace_bytes,
+                       uint32_t *err_flags, ep_stream_t stream);
+
 /* Static description of a status code. */
 EP_API const char *ep_status_string(ep_status_t status);
 

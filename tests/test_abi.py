@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.ep_abi_version() == 100
+    assert lib.ep_abi_version() == 101
     assert lib.ep_status_string(0) == b"ok"
     assert lib.ep_status_string(1) == b"invalid argument"
 
@@ -54,6 +54,9 @@ def test_rows_and_workspace(lib):
     s = ep.make_shape(16384, 4096, 128, 8, 8)
     assert ep.recv_rows(s) == 16384 * 8
     assert ep.layout_workspace_bytes(s) == 128 * 128 * 4  # 128 chunks x 128 experts x i32
+    # combine by source maps: a [T, k] row map and a [T, k] weight map, each rounded to 256 B
+    assert lib.ep_combine_src_workspace_bytes(ctypes.byref(s)) == 2 * 16384 * 8 * 4
+    assert lib.ep_combine_src_workspace_bytes(ctypes.byref(ep.make_shape(3, 8, 4, 1, 1))) == 2 * 256
 
 
 @pytest.mark.parametrize("bad", [
@@ -99,10 +102,20 @@ def test_host_checks_before_device(lib):
     big = _lib.Shape(8192, 64, 16, 8, 1, 0, 0)
     assert lib.ep_get_layout(ctypes.byref(big), *([fake] * 8), None, 0, None, None) == 1
     assert b"workspace" in lib.ep_last_error()
+    # combine by source maps: NULL maps, a small or misaligned workspace, a bad payload, fp8 with H % 128
+    ws = lib.ep_combine_src_workspace_bytes(ctypes.byref(s))
+    assert lib.ep_combine_src(ctypes.byref(s), fake, None, 0, None, None, fake, fake, fake, ws, None, None) == 1
+    assert lib.ep_combine_src(ctypes.byref(s), fake, None, 0, None, fake, fake, fake, fake, ws - 4, None, None) == 1
+    assert b"workspace" in lib.ep_last_error()
+    assert lib.ep_combine_src(ctypes.byref(s), fake, None, 0, None, fake, fake, fake, odd, ws, None, None) == 1
+    assert lib.ep_combine_src(ctypes.byref(s), fake, None, 5, None, fake, fake, fake, fake, ws, None, None) == 1
+    assert lib.ep_combine_src(ctypes.byref(s), fake, fake, 1, None, fake, fake, fake, fake, ws, None, None) == 1
+    assert lib.ep_combine_src(ctypes.byref(s128), fake, None, 1, None, fake, fake, fake, fake, ws, None, None) == 1
     # T == 0 is a no-op for dispatch / combine
     z = _lib.Shape(0, 64, 16, 4, 1, 0, 0)
     assert lib.ep_dispatch(ctypes.byref(z), *([None] * 3), 0, *([None] * 5)) == 0
     assert lib.ep_combine(ctypes.byref(z), *([None] * 6)) == 0
+    assert lib.ep_combine_src(ctypes.byref(z), None, None, 0, *([None] * 5), 0, None, None) == 0
 
 
 def test_product_path_does_not_use_the_oracle():
