@@ -335,9 +335,32 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             fn()
         inner[len(stages)].record()
 
+    # Each stage alone (its own graph, events inside it around the stage's
+    # kernels), timed after an L2 flush per call: the per-call figure of the
+    # method's measurement plan.  The variant ep_combine_src (combine through
+    # the expert-side source maps, per-row weights) is timed the same way.
+    row_w_d = torch.rand(plan.R, generator=gen, device="cuda", dtype=torch.float32)
+
+    def do_combine_src():
+        plan.combine_src(y_d, row_w_d)
+
+    alone_fns = [(n, fn) for n, fn, _, _ in stages] + [("combine_src", do_combine_src)]
+    alone_ev = {}
+
+    def bracket(n, fn):
+        def run():
+            alone_ev[n][0].record()
+            fn()
+            alone_ev[n][1].record()
+        return run
+
     graphs = {"step": capture(do_step)}
     if inner is not None:
         graphs["marked"] = capture(do_step_marked)
+        for n, fn in alone_fns:
+            alone_ev[n] = (torch.cuda.Event(enable_timing=True, external=True),
+                           torch.cuda.Event(enable_timing=True, external=True))
+            graphs["alone_" + n] = capture(bracket(n, fn))
     else:
         graphs.update({n: capture(fn) for n, fn, _, _ in stages})
     stream = torch.cuda.current_stream()
@@ -399,6 +422,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             evs = timed(graphs[n], args.steps)
             torch.cuda.synchronize()
             kernel_ms[n] = [a.elapsed_time(b) for a, b in evs]
+    alone_ms = {n: [] for n, _ in alone_fns} if inner is not None else {}
+    for n in alone_ms:
+        for _ in range(args.steps):
+            flush_l2()
+            graphs["alone_" + n].replay()
+            torch.cuda.synchronize()
+            alone_ms[n].append(alone_ev[n][0].elapsed_time(alone_ev[n][1]))
     per_kernel = {n: dict(us=round(statistics.median(kernel_ms[n]) * 1e3, 3),
                           us_mean=round(statistics.fmean(kernel_ms[n]) * 1e3, 3),
                           timed="inside the step graph" if inner is not None else "own graph, launch included")
@@ -456,6 +486,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     for name, r in per_kernel.items():
         gbs = nbytes[name] / (r["us"] * 1e-6) / 1e9
         r.update(bytes=nbytes[name], gbs=round(gbs, 1), frac_of_hbm=round(gbs / peak, 4))
+    # combine through the source maps reads each live row's (token, position,
+    # weight) record instead of the token-side slot and weight
+    nbytes_alone = dict(nbytes, combine_src=kbytes["combine"] - 8 * wl.T * wl.k + 12 * n_live)
+    alone = {}
+    for name, ms in alone_ms.items():
+        a_us = statistics.median(ms) * 1e3
+        a_gbs = nbytes_alone[name] / (a_us * 1e-6) / 1e9
+        alone[name] = dict(us=round(a_us, 3), bytes=nbytes_alone[name], gbs=round(a_gbs, 1),
+                           frac_of_hbm=round(a_gbs / peak, 4))
     dominant = max(names, key=lambda n: per_kernel[n]["us"])
     dk = per_kernel[dominant]
     ach = nbytes[dominant] / (dk["us_mean"] * 1e-6) / 1e9
@@ -474,6 +513,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine",
                    "parallelism": f"replicas x{world}"},
         "kernels": per_kernel,
+        "kernels_alone": dict(alone, how="each stage in its own graph with CUDA events inside it around the "
+                                          "stage, L2 flushed before every call, median of K calls"),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dominant], "peak_source": f"{peak_kind} hbm_gbs"},
