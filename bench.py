@@ -14,10 +14,13 @@ Timing: inputs resident in HBM; the L2 (129 MB) is flushed before every timed
 step by writing a 512 MB buffer and then reading another 512 MB (so it holds
 only clean, unrelated lines); each step is one CUDA-graph replay of the three
 calls, bracketed by CUDA events on the launching stream.  Per-kernel times
-come from a second graph of the same step with event-record nodes between the
-kernels (one graph per kernel where torch lacks such events).  e2e: the same
-step through the
-public API with pinned host inputs, host->device copies and the device->host
+come from K more steps launched without a graph, with a CUDA event recorded
+on the launching stream before and after every call; all of it is enqueued
+behind the flush, so the calls run back to back as in the graph.  (Event
+nodes inside a graph gave per-kernel times that grew by up to 2 us with the
+number of graphs the process had instantiated, for the same kernel.)  Each
+stage is also timed alone, after its own flush.  e2e: the same step through
+the public API with pinned host inputs, host->device copies and the device->host
 read of the combined output inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -321,48 +324,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             fn()
         return g
 
-    # Event-record nodes between the kernels of a second step graph time each
-    # kernel inside the step; torch without such events falls back to one
-    # graph per kernel (launch latency included).
-    try:
-        inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stages) + 1)]
-    except TypeError:
-        inner = None
-
-    def do_step_marked():
-        for q, (_, fn, _, _) in enumerate(stages):
-            inner[q].record()
-            fn()
-        inner[len(stages)].record()
-
-    # Each stage alone (its own graph, events inside it around the stage's
-    # kernels), timed after an L2 flush per call: the per-call figure of the
-    # method's measurement plan.  The variant ep_combine_src (combine through
-    # the expert-side source maps, per-row weights) is timed the same way.
+    # Each stage alone after an L2 flush per call is the per-call figure of
+    # the method's measurement plan; the variant ep_combine_src (combine
+    # through the expert-side source maps, per-row weights) is timed the same
+    # way.
     row_w_d = torch.rand(plan.R, generator=gen, device="cuda", dtype=torch.float32)
 
     def do_combine_src():
         plan.combine_src(y_d, row_w_d)
 
     alone_fns = [(n, fn) for n, fn, _, _ in stages] + [("combine_src", do_combine_src)]
-    alone_ev = {}
-
-    def bracket(n, fn):
-        def run():
-            alone_ev[n][0].record()
-            fn()
-            alone_ev[n][1].record()
-        return run
-
     graphs = {"step": capture(do_step)}
-    if inner is not None:
-        graphs["marked"] = capture(do_step_marked)
-        for n, fn in alone_fns:
-            alone_ev[n] = (torch.cuda.Event(enable_timing=True, external=True),
-                           torch.cuda.Event(enable_timing=True, external=True))
-            graphs["alone_" + n] = capture(bracket(n, fn))
-    else:
-        graphs.update({n: capture(fn) for n, fn, _, _ in stages})
     stream = torch.cuda.current_stream()
 
     def timed(g, n):
@@ -409,29 +381,33 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     wall = time.perf_counter() - t0
     step_ms = [a.elapsed_time(b) for a, b in step_evs]
 
-    # ---- per-kernel times, same flush discipline, K more steps
+    # ---- per-kernel times, same flush discipline, K more steps: the calls of
+    # a step launched one by one with an event on the stream between them,
+    # all enqueued behind the flush so that they run back to back.
     kernel_ms = {n: [] for n in names}
-    if inner is not None:
-        for _ in range(args.steps):
-            timed(graphs["marked"], 1)
-            torch.cuda.synchronize()
-            for q, n in enumerate(names):
-                kernel_ms[n].append(inner[q].elapsed_time(inner[q + 1]))
-    else:
-        for n in names:
-            evs = timed(graphs[n], args.steps)
-            torch.cuda.synchronize()
-            kernel_ms[n] = [a.elapsed_time(b) for a, b in evs]
-    alone_ms = {n: [] for n, _ in alone_fns} if inner is not None else {}
-    for n in alone_ms:
+    for _ in range(args.steps):
+        flush_l2()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+        for q, (_, fn, _, _) in enumerate(stages):
+            evs[q].record(stream)
+            fn()
+        evs[-1].record(stream)
+        torch.cuda.synchronize()
+        for q, n in enumerate(names):
+            kernel_ms[n].append(evs[q].elapsed_time(evs[q + 1]))
+    alone_ms = {n: [] for n, _ in alone_fns}
+    for n, fn in alone_fns:
         for _ in range(args.steps):
             flush_l2()
-            graphs["alone_" + n].replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
             torch.cuda.synchronize()
-            alone_ms[n].append(alone_ev[n][0].elapsed_time(alone_ev[n][1]))
+            alone_ms[n].append(a.elapsed_time(b))
     per_kernel = {n: dict(us=round(statistics.median(kernel_ms[n]) * 1e3, 3),
                           us_mean=round(statistics.fmean(kernel_ms[n]) * 1e3, 3),
-                          timed="inside the step graph" if inner is not None else "own graph, launch included")
+                          timed="inside a step launched call by call, events on the stream between the calls")
                   for n in names}
 
     # ---- e2e through the public API with host buffers: every step copies its
@@ -513,8 +489,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine",
                    "parallelism": f"replicas x{world}"},
         "kernels": per_kernel,
-        "kernels_alone": dict(alone, how="each stage in its own graph with CUDA events inside it around the "
-                                          "stage, L2 flushed before every call, median of K calls"),
+        "kernels_alone": dict(alone, how="each stage launched alone between two CUDA events on the stream, "
+                                          "L2 flushed before every call, median of K calls"),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dominant], "peak_source": f"{peak_kind} hbm_gbs"},
