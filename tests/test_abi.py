@@ -126,3 +126,23 @@ def test_product_path_does_not_use_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_plain_c_client_compiles_links_and_runs(tmp_path):
+    """include/ep.h is a C header: a C11 program using it builds with
+    warnings as errors, links against the library and passes its host-side
+    checks."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    path = ep.library_path()
+    exe = tmp_path / "abi_client"
+    src = os.path.join(os.path.dirname(__file__), "abi_client.c")
+    inc = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, src, "-o", str(exe),
+                    path, "-Wl,-rpath," + os.path.dirname(path)], check=True, capture_output=True, text=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "abi client ok" in res.stdout
