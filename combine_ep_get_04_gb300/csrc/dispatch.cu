@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
 
     // ------------------------------------------------------------ quantisers
     const int qw = warp - 2;
+    const float r448 = recip_448();
     for (int64_t i = 0; i < n_mine; ++i) {
         const int s = (int)(i % NS);
         const int o = (int)(i % NSO);
@@ -328,9 +329,10 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
             float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-            const float sc = block_scale(m, a.ue8m0 != 0);
-            const uint32_t q01 = pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
-            const uint32_t q23 = pack_e4m3x2(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
+            const float sc = block_scale(m, a.ue8m0 != 0, r448);
+            const float rs = __frcp_rn(sc);
+            const uint32_t q01 = pack_e4m3x2(quotient_rn(x0, sc, rs), quotient_rn(x1, sc, rs));
+            const uint32_t q23 = pack_e4m3x2(quotient_rn(x2, sc, rs), quotient_rn(x3, sc, rs));
             *reinterpret_cast<uint32_t*>(ob + b * 128 + lane * 4) = q01 | (q23 << 16);
             if (lane == 0) {
                 if (a.ue8m0) {

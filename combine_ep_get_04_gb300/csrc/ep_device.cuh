@@ -147,11 +147,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// x / d rounded to nearest even, from rd = RN32(1 / d): q0 = RN(x * rd), the
+// residual r = x - q0 * d (exact, one fused multiply-add), then RN(q0 + r * rd).
+// This is Markstein's quotient correction (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Develop. 34(1), 1990): with rd the correctly rounded reciprocal and q0 within
+// one ulp of x / d, the corrected quotient is the correctly rounded one as long
+// as nothing underflows.  It is used only with d a block scale (a normal number
+// in [2^-23, 2^120]) or 448, and x a bf16 value no larger in magnitude than
+// the amax the scale came from: there the scale and every e4m3 code equal
+// those of the IEEE quotient, for every bf16 amax and every such x (checked
+// exhaustively against __fdiv_rn on the GPU, and the method against C's
+// division on the CPU).  The sign comes from x, so that -0 stays -0.
+__device__ __forceinline__ float quotient_rn(float x, float d, float rd) {
+    const float q0 = __fmul_rn(x, rd);
+    const float r = __fmaf_rn(-q0, d, x);
+    return copysignf(__fmaf_rn(r, rd, q0), x);
+}
+
+// RN32(1 / 448), the reciprocal block_scale works with.
+__device__ __forceinline__ float recip_448() { return __frcp_rn(448.0f); }
+
 // Scale of a 128-channel block: v = RN32(max(amax, 1e-4) / 448); with UE8M0
 // scales, the smallest power of two >= v (exact: bump the exponent unless the
-// mantissa is zero; v is a positive normal number here).
-__device__ __forceinline__ float block_scale(float amax, bool ue8m0) {
-    float v = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+// mantissa is zero; v is a positive normal number here).  r448 = recip_448().
+__device__ __forceinline__ float block_scale(float amax, bool ue8m0, float r448) {
+    float v = quotient_rn(fmaxf(amax, 1e-4f), 448.0f, r448);
     if (ue8m0) {
         uint32_t b = __float_as_uint(v);
         if (b & 0x007fffffu) b = (b & 0x7f800000u) + 0x00800000u;

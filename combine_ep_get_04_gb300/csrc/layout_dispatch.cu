@@ -14,8 +14,10 @@
 // of smaller experts (the packed offset of e) and the ids before (t, j) equal
 // to e (the rank) -- the same deterministic source order as ep_get_layout.
 // One extra CTA builds the full histogram and scan for counts and offsets.
-// Each CTA then writes its share of the layout outputs and copies (bf16) or
-// quantises (fp8) the slice into the k receive rows with bulk stores.
+// Each CTA then writes its share of the layout outputs and copies the slice
+// into the k receive rows (bf16: bulk stores issued from k warps at once) or
+// quantises it (fp8: each warp stores the codes and scale of its 128-channel
+// blocks from registers straight into the k rows).
 #include "ep.h"
 #include "ep_device.cuh"
 #include "ep_kernels.h"
@@ -30,9 +32,11 @@ namespace ep {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarpsF = 8;
+constexpr int kWarpsF = 16;
 constexpr int kThreadsF = kWarpsF * 32;
 constexpr int kIdsPerThread = (int)(kFusedMaxN / kThreadsF);   // every id of the batch, in registers
+constexpr int kExpPerThread = 1024 / kThreadsF;                // experts per thread in the scan (E <= 1024)
+constexpr int kCopyChunk = 8;                                  // copies counted together (k <= 32)
 
 struct FusedArgs {
     const int32_t* topk_idx;
@@ -55,24 +59,25 @@ struct FusedArgs {
     int ue8m0;               // power-of-two scales stored as exponent bytes
     int nb;                  // H / 128 (fp8)
     int nblk;                // 128-channel blocks per unit (fp8)
-    int scale_bulk;          // scale rows stored with a bulk copy
     uint32_t in_bytes;       // bf16 bytes of one unit
-    uint32_t in_stride;      // in_bytes rounded up to 128
 };
+
+// Shared memory: the mbarrier, then these int32 arrays, then the x slice.
+__host__ __device__ constexpr uint32_t fused_head_bytes(int E) {
+    return (16u + (32u + 32u + 32u * kWarpsF + 8u) * 4u + 8u * (uint32_t)E + 127u) & ~127u;
+}
 
 // One CTA per unit u = (t, sl).
 __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     int32_t* tok_e = reinterpret_cast<int32_t*>(smem + 16);      // [32] experts of this token
-    int32_t* rank_s = tok_e + 32;                                 // [32] rank of each copy
-    int32_t* slot_s = rank_s + 32;                                // [32] receive row of each copy
-    int32_t* wsum_s = slot_s + 32;                                // [8]
-    int32_t* misc_s = wsum_s + 8;                                 // [0] valid ids, [1] flags, [2] scan total
+    int32_t* slot_s = tok_e + 32;                                 // [32] receive row of each copy
+    int32_t* part_s = slot_s + 32;                                // [kWarpsF][32] per-warp counts per copy
+    int32_t* misc_s = part_s + 32 * kWarpsF;                      // [0] valid ids, [1] flags, [2] scan total
     int32_t* cnt_s = misc_s + 8;                                  // [E]
     int32_t* off_s = cnt_s + a.E;                                 // [E]
-    unsigned char* in_st = smem + ((16 + (32 * 3 + 16) * 4 + 8 * a.E + 127) & ~127);
-    unsigned char* out_st = in_st + a.in_stride;                  // fp8 codes, then scales
+    unsigned char* in_st = smem + fused_head_bytes(a.E);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -112,10 +117,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         misc_s[1] = 0;
     }
     for (int e = tid; e < a.E; e += kThreadsF) cnt_s[e] = 0;
-    if (tid < 32) {
-        rank_s[tid] = 0;
-        tok_e[tid] = my_tok_e;
-    }
+    if (tid < 32) tok_e[tid] = my_tok_e;
     __syncthreads();
     if (hist_cta) {
         // counts, offsets and partition sums of all experts; bad ids
@@ -133,10 +135,10 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         }
         if (bad) atomicOr(&misc_s[1], (int)kErrBadExpert);
         __syncthreads();
-        int32_t v[4], sum = 0;
+        int32_t v[kExpPerThread], sum = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = 4 * tid + q;
+        for (int q = 0; q < kExpPerThread; ++q) {
+            const int e = kExpPerThread * tid + q;
             v[q] = e < a.E ? cnt_s[e] : 0;
             sum += v[q];
         }
@@ -146,24 +148,24 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
             const int32_t o = __shfl_up_sync(kFull, incl, d);
             if (lane >= d) incl += o;
         }
-        if (lane == 31) wsum_s[warp] = incl;
+        if (lane == 31) part_s[warp] = incl;
         __syncthreads();
         if (warp == 0) {
-            const int32_t ws = lane < kWarpsF ? wsum_s[lane] : 0;
+            const int32_t ws = lane < kWarpsF ? part_s[lane] : 0;
             int32_t wincl = ws;
 #pragma unroll
             for (int d = 1; d < kWarpsF; d <<= 1) {
                 const int32_t o = __shfl_up_sync(kFull, wincl, d);
                 if (lane >= d) wincl += o;
             }
-            if (lane < kWarpsF) wsum_s[lane] = wincl - ws;
+            if (lane < kWarpsF) part_s[lane] = wincl - ws;
             if (lane == kWarpsF - 1) misc_s[2] = wincl;
         }
         __syncthreads();
-        int32_t run = wsum_s[warp] + incl - sum;
+        int32_t run = part_s[warp] + incl - sum;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = 4 * tid + q;
+        for (int q = 0; q < kExpPerThread; ++q) {
+            const int e = kExpPerThread * tid + q;
             if (e < a.E) off_s[e] = run;
             run += v[q];
         }
@@ -189,20 +191,32 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
     // Slot of copy j of this token, from two counts over all ids:
     //   lt_j = valid ids with a smaller expert than e_j (= offsets[e_j]),
     //   eq_j = ids before (t, j) with expert e_j      (= rank of the copy),
-    // packed as lt << 16 | eq (both <= kFusedMaxN) and summed over the CTA.
-    for (int j = 0; j < a.k; ++j) {
-        const int ej = tok_e[j];
-        int c = 0;
+    // packed as lt << 16 | eq (both <= kFusedMaxN).  Eight copies are counted
+    // together (independent sums), reduced per warp and kept per warp; the
+    // warps' partial counts are added after the barrier.
+    for (int j0 = 0; j0 < a.k; j0 += kCopyChunk) {
+        int ej[kCopyChunk], c[kCopyChunk];
+#pragma unroll
+        for (int jj = 0; jj < kCopyChunk; ++jj) {
+            ej[jj] = j0 + jj < a.k ? tok_e[j0 + jj] : -2;
+            c[jj] = 0;
+        }
 #pragma unroll
         for (int q = 0; q < kIdsPerThread; ++q) {
             if (q * kThreadsF >= a.N) break;
             const int e = ids[q];
             const int n = q * kThreadsF + tid;
-            c += (e >= 0 && e < ej) ? 0x10000 : 0;
-            c += (e == ej && n < tk0 + j) ? 1 : 0;
+#pragma unroll
+            for (int jj = 0; jj < kCopyChunk; ++jj) {
+                c[jj] += (e >= 0 && e < ej[jj]) ? 0x10000 : 0;
+                c[jj] += (e == ej[jj] && n < tk0 + j0 + jj) ? 1 : 0;
+            }
         }
-        c = __reduce_add_sync(kFull, c);
-        if (lane == 0 && c) atomicAdd(&rank_s[j], c);
+#pragma unroll
+        for (int jj = 0; jj < kCopyChunk; ++jj) {
+            const int r = __reduce_add_sync(kFull, c[jj]);
+            if (lane == 0 && j0 + jj < 32) part_s[warp * 32 + j0 + jj] = r;
+        }
     }
     // Counts this CTA needs to mark rows that hold no copy: per expert it
     // covers (capacity), or the number of valid ids (packed).
@@ -234,7 +248,10 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         const int e = tok_e[tid];
         int32_t slot = -1;
         if (e >= 0) {
-            const int32_t lt = rank_s[tid] >> 16, rank = rank_s[tid] & 0xffff;
+            int32_t packed = 0;
+#pragma unroll
+            for (int w = 0; w < kWarpsF; ++w) packed += part_s[w * 32 + tid];
+            const int32_t lt = packed >> 16, rank = packed & 0xffff;
             if (a.mode == 0) {
                 slot = lt + rank;
             } else if (rank < a.cap) {
@@ -270,60 +287,57 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
             }
         }
     }
-    __syncthreads();
 
-    // Copy or quantise the slice into the k receive rows.
+    // Copy or quantise the slice into the k receive rows (the barrier also
+    // publishes slot_s).
     const bool ok = __syncthreads_and(mbar_wait(bar, 0)) != 0;
     if (ok) {
         if (!a.fp8) {
-            if (warp == 0) {
-                const int32_t slot = lane < a.k ? slot_s[lane] : -1;
-                if (slot >= 0) {
-                    bulk_store(a.recv + (int64_t)slot * a.H * 2 + (int64_t)sl * a.in_bytes, in_st, a.in_bytes);
+            // copy j is issued by lane 0 of warp j % kWarpsF: up to kWarpsF bulk stores start together
+            if (lane == 0) {
+                for (int j = warp; j < a.k; j += kWarpsF) {
+                    const int32_t slot = slot_s[j];
+                    if (slot >= 0) {
+                        bulk_store(a.recv + (int64_t)slot * a.H * 2 + (int64_t)sl * a.in_bytes, in_st, a.in_bytes);
+                    }
                 }
                 bulk_commit();
-                bulk_wait_all();
+                bulk_wait_read<0>();   // the slice stays in shared memory until every copy has read it
             }
         } else {
-            const uint32_t q_bytes = (uint32_t)a.nblk * 128u;
-            float* oscale = reinterpret_cast<float*>(out_st + q_bytes);
+            // Warp per 128-channel block: amax, scale, codes; lane l holds the
+            // codes of channels 4l..4l+3 and stores them (and lane j < k the
+            // block's scale) into every copy's row.
+            const float r448 = recip_448();
+            const int64_t col0 = (int64_t)sl * a.nblk * 128;
+            const int64_t s_col0 = (int64_t)sl * a.nblk;
             for (int b = warp; b < a.nblk; b += kWarpsF) {
                 const uint2 v = *reinterpret_cast<const uint2*>(in_st + b * 256 + lane * 8);
                 const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
                 float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
                 for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-                const float sc = block_scale(m, a.ue8m0 != 0);
-                const uint32_t q01 = pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
-                const uint32_t q23 = pack_e4m3x2(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
-                *reinterpret_cast<uint32_t*>(out_st + b * 128 + lane * 4) = q01 | (q23 << 16);
-                if (lane == 0) {
-                    if (a.ue8m0) {
-                        out_st[q_bytes + b] = ue8m0_byte(sc);
-                    } else {
-                        oscale[b] = sc;
+                const float sc = block_scale(m, a.ue8m0 != 0, r448);
+                const float rs = __frcp_rn(sc);
+                const uint32_t q01 = pack_e4m3x2(quotient_rn(x0, sc, rs), quotient_rn(x1, sc, rs));
+                const uint32_t q23 = pack_e4m3x2(quotient_rn(x2, sc, rs), quotient_rn(x3, sc, rs));
+                const uint32_t codes = q01 | (q23 << 16);
+                const int64_t col = col0 + b * 128 + lane * 4;
+                for (int j = 0; j < a.k; ++j) {
+                    const int32_t slot = slot_s[j];
+                    if (slot >= 0) *reinterpret_cast<uint32_t*>(a.recv + (int64_t)slot * a.H + col) = codes;
+                }
+                if (lane < a.k) {
+                    const int32_t slot = slot_s[lane];
+                    if (slot >= 0) {
+                        const int64_t si = (int64_t)slot * a.nb + s_col0 + b;
+                        if (a.ue8m0) {
+                            static_cast<uint8_t*>(a.recv_s)[si] = ue8m0_byte(sc);
+                        } else {
+                            static_cast<float*>(a.recv_s)[si] = sc;
+                        }
                     }
                 }
-            }
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (warp == 0) {
-                const int32_t slot = lane < a.k ? slot_s[lane] : -1;
-                if (slot >= 0) {
-                    bulk_store(a.recv + (int64_t)slot * a.H + (int64_t)sl * a.nblk * 128, out_st, q_bytes);
-                    const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.nblk;
-                    if (a.ue8m0) {
-                        uint8_t* edst = static_cast<uint8_t*>(a.recv_s) + s0;
-                        for (int b = 0; b < a.nblk; ++b) edst[b] = out_st[q_bytes + b];
-                    } else if (a.scale_bulk) {
-                        bulk_store(static_cast<float*>(a.recv_s) + s0, oscale, (uint32_t)a.nblk * 4u);
-                    } else {
-                        float* sdst = static_cast<float*>(a.recv_s) + s0;
-                        for (int b = 0; b < a.nblk; ++b) sdst[b] = oscale[b];
-                    }
-                }
-                bulk_commit();
-                bulk_wait_all();
             }
         }
     } else if (tid == 0) {
@@ -383,17 +397,13 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
         a.nb = f.H / 128;
         a.slices = pick_divisor(f.T, a.nb, 64, 2, (int64_t)EP_FUSED_UNITS_PER_SM * num_sms);
         a.nblk = a.nb / a.slices;
-        a.scale_bulk = (a.nb % 4 == 0) && (a.nblk % 4 == 0);
         a.in_bytes = (uint32_t)a.nblk * 256u;
     } else {
         const int64_t vec16 = (int64_t)f.H * 2 / 16;
         a.slices = pick_divisor(f.T, vec16, 1024, 64, (int64_t)EP_FUSED_UNITS_PER_SM * num_sms);
         a.in_bytes = (uint32_t)(vec16 / a.slices * 16);
     }
-    a.in_stride = (a.in_bytes + 127u) & ~127u;
-    const size_t head = (16 + (32 * 3 + 16) * 4 + 8 * (size_t)f.E + 127) & ~(size_t)127;
-    const size_t out_bytes = f.fp8 ? (((size_t)a.nblk * 132 + 127) & ~(size_t)127) : 0;
-    const size_t smem = head + a.in_stride + out_bytes;
+    const size_t smem = fused_head_bytes(f.E) + ((a.in_bytes + 127u) & ~127u);
     cudaError_t err = cudaFuncSetAttribute(layout_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
