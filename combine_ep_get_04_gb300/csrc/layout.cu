@@ -126,23 +126,16 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(LayoutParams p) {
             }
         }
     } else {
-        if (ranks_chunk) {
-            if (my_n < N) {
-                my_e = __ldg(p.topk_idx + my_n);
-                if (my_e < -1 || my_e >= E) {
-                    bad = true;
-                    my_e = -1;
-                }
-            }
-            const uint32_t peers = __match_any_sync(kFull, my_e);
-            my_in_warp = __popc(peers & lanemask_lt());
-            if (my_e >= 0 && lane == __ffs(peers) - 1) tab[warp * E + my_e] = (uint16_t)__popc(peers);
-        }
+        // This thread's entry is loaded first; it is used only after the
+        // column sums below, so both latencies overlap.
+        if (ranks_chunk && my_n < N) my_e = __ldg(p.topk_idx + my_n);
         // tpe threads per expert column of the histogram, each summing every
-        // tpe-th chunk with eight independent loads in flight.
+        // tpe-th chunk with eight independent loads in flight.  Consecutive
+        // threads take consecutive experts of one chunk, so each warp load
+        // reads one or two whole lines of the table every CTA reads.
         const int tpe = max(1, kThreads / E);
-        const int e = tid / tpe, sub = tid - e * tpe;
-        if (e < E) {
+        const int e = tid % E, sub = tid / E;
+        if (sub < tpe) {
             int32_t before = 0, total = 0;
             int cc = sub;
             for (; cc + 7 * tpe < p.num_chunks; cc += 8 * tpe) {
@@ -162,6 +155,15 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(LayoutParams p) {
             }
             if (before) atomicAdd(&base_s[e], before);
             if (total) atomicAdd(&cnt_s[e], total);
+        }
+        if (ranks_chunk) {
+            if (my_e < -1 || my_e >= E) {
+                bad = true;
+                my_e = -1;
+            }
+            const uint32_t peers = __match_any_sync(kFull, my_e);
+            my_in_warp = __popc(peers & lanemask_lt());
+            if (my_e >= 0 && lane == __ffs(peers) - 1) tab[warp * E + my_e] = (uint16_t)__popc(peers);
         }
     }
     if (bad) atomicOr(&flags_s, (int)kErrBadExpert);
