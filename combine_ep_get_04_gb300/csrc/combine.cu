@@ -89,26 +89,48 @@ __device__ __forceinline__ float ue8m0_value(uint32_t e) {
     return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
 }
 
-// Accumulates w * (value(code) * s) for 16 fp8 codes.
-__device__ __forceinline__ void accumulate_fp8(float (&acc)[16], float w, float s, const uint4& v) {
+// Two fp32 lanes in one 64-bit register, and the packed two-wide fp32
+// multiply and add of sm_100+ (each lane rounded to nearest on its own, no
+// flush to zero: exactly two __fmul_rn / __fadd_rn, in half the instructions).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_pair_bf16x2(uint64_t pair) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(pair));
+    return pack_bf16x2(lo, hi);
+}
+
+// Accumulates w * (value(code) * s) for 16 fp8 codes, as 8 lane pairs.
+__device__ __forceinline__ void accumulate_fp8(uint64_t (&acc)[8], uint64_t w2, uint64_t s2, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float2 a = e4m3x2_to_float2((uint16_t)(words[q] & 0xffffu));
         const float2 b = e4m3x2_to_float2((uint16_t)(words[q] >> 16));
-        acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], __fmul_rn(w, __fmul_rn(a.x, s)));
-        acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], __fmul_rn(w, __fmul_rn(a.y, s)));
-        acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], __fmul_rn(w, __fmul_rn(b.x, s)));
-        acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], __fmul_rn(w, __fmul_rn(b.y, s)));
+        acc[2 * q] = add_f32x2(acc[2 * q], mul_f32x2(w2, mul_f32x2(f32x2(a.x, a.y), s2)));
+        acc[2 * q + 1] = add_f32x2(acc[2 * q + 1], mul_f32x2(w2, mul_f32x2(f32x2(b.x, b.y), s2)));
     }
 }
 
-__device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4& v) {
+// Accumulates w * y for 8 bf16 values, as 4 lane pairs.
+__device__ __forceinline__ void accumulate(uint64_t (&acc)[4], uint64_t w2, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(w, bf16_lo(words[q])));
-        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __fmul_rn(w, bf16_hi(words[q])));
+        acc[q] = add_f32x2(acc[q], mul_f32x2(w2, f32x2(bf16_lo(words[q]), bf16_hi(words[q]))));
     }
 }
 
@@ -228,25 +250,26 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
             unsigned char* dst = a.out + (t * a.row_bytes + (int64_t)sl * a.slice_bytes) * 2;
             for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
                 const int blk = (ch * 16) / 128;
-                float acc[16];
+                uint64_t acc[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+                for (int q = 0; q < 8; ++q) acc[q] = 0;   // +0.0f in both lanes
                 for (int j = 0; j < a.k; ++j) {
                     if (valid & (1u << j)) {
                         const uint4 v =
                             *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
-                        accumulate_fp8(acc, w_s[s * 32 + j], sc_s[(s * 32 + j) * kMaxSliceBlocks + blk], v);
+                        const float w = w_s[s * 32 + j], sc = sc_s[(s * 32 + j) * kMaxSliceBlocks + blk];
+                        accumulate_fp8(acc, f32x2(w, w), f32x2(sc, sc), v);
                     }
                 }
                 uint4 o0, o1;
-                o0.x = pack_bf16x2(acc[0], acc[1]);
-                o0.y = pack_bf16x2(acc[2], acc[3]);
-                o0.z = pack_bf16x2(acc[4], acc[5]);
-                o0.w = pack_bf16x2(acc[6], acc[7]);
-                o1.x = pack_bf16x2(acc[8], acc[9]);
-                o1.y = pack_bf16x2(acc[10], acc[11]);
-                o1.z = pack_bf16x2(acc[12], acc[13]);
-                o1.w = pack_bf16x2(acc[14], acc[15]);
+                o0.x = pack_pair_bf16x2(acc[0]);
+                o0.y = pack_pair_bf16x2(acc[1]);
+                o0.z = pack_pair_bf16x2(acc[2]);
+                o0.w = pack_pair_bf16x2(acc[3]);
+                o1.x = pack_pair_bf16x2(acc[4]);
+                o1.y = pack_pair_bf16x2(acc[5]);
+                o1.z = pack_pair_bf16x2(acc[6]);
+                o1.w = pack_pair_bf16x2(acc[7]);
                 *reinterpret_cast<uint4*>(dst + ch * 32) = o0;
                 *reinterpret_cast<uint4*>(dst + ch * 32 + 16) = o1;
             }
@@ -256,20 +279,19 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
         }
         unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
         for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
-            float acc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
             for (int j = 0; j < a.k; ++j) {
                 if (valid & (1u << j)) {
                     const uint4 v = *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
-                    accumulate(acc, w_s[s * 32 + j], v);
+                    const float w = w_s[s * 32 + j];
+                    accumulate(acc, f32x2(w, w), v);
                 }
             }
             uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
+            o.x = pack_pair_bf16x2(acc[0]);
+            o.y = pack_pair_bf16x2(acc[1]);
+            o.z = pack_pair_bf16x2(acc[2]);
+            o.w = pack_pair_bf16x2(acc[3]);
             *reinterpret_cast<uint4*>(dst + ch * 16) = o;
         }
         __syncwarp();
