@@ -387,6 +387,8 @@ FUSED_CASES = [
     (256, 7168, 256, 8, 32, None, True, 0.0, False),     # N = 2048, the fused limit
     (300, 7168, 256, 8, 32, None, True, 0.0, False),     # beyond it: the two-call path
     (17, 2048, 32, 8, 4, 3, False, 0.05, True),
+    (60, 1024, 64, 32, 4, None, True, 0.05, False),      # fp8, k = 32: four passes of eight copies
+    (96, 2048, 128, 16, 8, 8, True, 0.0, True),          # fp8 into a capacity buffer that overflows
 ]
 
 
