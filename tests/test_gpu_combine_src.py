@@ -158,3 +158,41 @@ def test_combine_src_after_gpu_dispatch_round_trip():
     recv, _, recv_w = plan.dispatch(bf16_dev(d["x"]), dev(w))
     out = plan.combine_src(recv, recv_w)
     np.testing.assert_array_equal(bits(out), d["x"])
+
+
+def _random_bf16_rows(rng, R, H):
+    """Finite bf16 bit patterns, magnitudes in [2^-6, 2^2), random signs: cheap at
+    full size (one draw of 16-bit integers)."""
+    raw = rng.integers(0, 1 << 16, size=(R, H), dtype=np.uint16)
+    exp = ((raw >> np.uint16(7)) & np.uint16(0x7)) + np.uint16(121)
+    return (raw & np.uint16(0x807F)) | (exp << np.uint16(7))
+
+
+@pytest.mark.parametrize("name", ["prefill", "skewed"])
+def test_combine_src_full_size_sampled(name):
+    """Full-size workload in the benchmark's launch configuration: the oracle's
+    layout gives the source maps, seeded numpy the expert outputs and row
+    weights.  Every output token equals the slot_of combine bit for bit, and 64
+    sampled tokens match the oracle, which is given just those tokens' rows
+    (renumbered)."""
+    d = W.make(name)
+    wl = d["wl"]
+    L = oracle.layout(d["topk_idx"], wl.E, wl.P)
+    rng = np.random.default_rng(17)
+    y = _random_bf16_rows(rng, wl.R, wl.H)
+    row_w = rng.random(wl.R).astype(np.float32)
+    st, sk = L["src_token"], L["src_k"]
+    plan = ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, None)
+    y_d = bf16_dev(y)
+    out = plan.combine_src(y_d, dev(row_w), dev(st), dev(sk)).clone()
+    topk_w = np.where(L["slot_of"] >= 0, row_w[np.maximum(L["slot_of"], 0)], 0).astype(np.float32)
+    ref = plan.combine(y_d, dev(topk_w), out=torch.empty_like(out), slot_of=dev(L["slot_of"]))
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert int(plan.layout_out.err_flags.item()) == 0
+    toks = np.sort(np.random.default_rng(3).choice(wl.T, size=64, replace=False))
+    slot = L["slot_of"][toks]
+    rows = slot[slot >= 0]
+    new_t = np.searchsorted(toks, st[rows]).astype(np.int32)
+    o = oracle.combine_src(y[rows], row_w[rows], new_t, sk[rows], len(toks), wl.k)
+    assert_combine_close(bits(out)[toks], o)
