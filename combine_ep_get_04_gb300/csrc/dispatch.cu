@@ -16,6 +16,22 @@
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
+// Units each CTA takes when there are more units than one resident wave of
+// CTAs holds (0: a persistent grid of one wave, every CTA looping over an
+// equal share).  The SMs do not get equal shares of memory bandwidth (per-CTA
+// end times of one persistent bf16 dispatch ranged from 50 to 83 us on the
+// prefill workload and from 81 to 201 us on the group-limited one, by SM), so
+// a persistent grid ends on its slowest SMs; a grid of short CTAs lets the
+// block scheduler give more of them to the SMs that free up first.  Tuned:
+// bf16 one unit per CTA (prefill 88.5 -> 80.3 us, group-limited 202 -> 179
+// us), fp8 six (its ten-warp CTAs cost more to start; skewed 98.8 -> 96.8 us).
+#ifndef EP_BF16_UNITS_PER_CTA
+#define EP_BF16_UNITS_PER_CTA 1
+#endif
+#ifndef EP_FP8_UNITS_PER_CTA
+#define EP_FP8_UNITS_PER_CTA 6
+#endif
+
 // Pipeline shape (compile-time; the defaults are the tuned values).
 #ifndef EP_BF16_STAGES
 #define EP_BF16_STAGES 4
@@ -402,6 +418,11 @@ cudaError_t launch_dispatch_bf16(const DispatchParams& p, int num_sms, cudaStrea
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms * per_sm;
     if (grid > a.units) grid = a.units;
+    if (EP_BF16_UNITS_PER_CTA > 0) {
+        const int64_t upc = EP_BF16_UNITS_PER_CTA > 0 ? EP_BF16_UNITS_PER_CTA : 1;
+        const int64_t g2 = (a.units + upc - 1) / upc;
+        if (g2 > grid) grid = g2;
+    }
     return launch_kernel(grid >= a.units, kern, dim3((unsigned)grid), dim3(32), smem, stream, a);
 }
 
@@ -438,6 +459,11 @@ cudaError_t launch_dispatch_fp8(const DispatchParams& p, int num_sms, cudaStream
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms * per_sm;
     if (grid > a.units) grid = a.units;
+    if (EP_FP8_UNITS_PER_CTA > 0) {
+        const int64_t upc = EP_FP8_UNITS_PER_CTA > 0 ? EP_FP8_UNITS_PER_CTA : 1;
+        const int64_t g2 = (a.units + upc - 1) / upc;
+        if (g2 > grid) grid = g2;
+    }
     return launch_kernel(grid >= a.units, kern, dim3((unsigned)grid), dim3(kFp8Threads), smem, stream, a);
 }
 
