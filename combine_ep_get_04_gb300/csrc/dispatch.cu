@@ -49,7 +49,7 @@
 #define EP_FP8_OUT_STAGES 3
 #endif
 #ifndef EP_FP8_QUANT_WARPS
-#define EP_FP8_QUANT_WARPS 8
+#define EP_FP8_QUANT_WARPS 12
 #endif
 #ifndef EP_FP8_SLICE_BLOCKS
 #define EP_FP8_SLICE_BLOCKS 64        // 128-channel blocks per fp8 unit at most
