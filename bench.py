@@ -10,10 +10,13 @@ Metric: effective HBM GB/s of the step = algorithmic bytes (what the method
 must move; see algorithmic_bytes) / device time, plus per-kernel us/call, GB/s
 and fraction of the measured HBM copy bandwidth.
 
-Timing: inputs resident in HBM; the L2 (129 MB) is flushed before every timed
-step by writing a 512 MB buffer and then reading another 512 MB (so it holds
-only clean, unrelated lines); each step is one CUDA-graph replay of the three
-calls, bracketed by CUDA events on the launching stream.  Per-kernel times
+Timing: inputs resident in HBM.  The K timed steps run back to back in one
+CUDA graph between two CUDA events, step i on set i % n of its own inputs and
+outputs, with n sets whose data together is at least four times the 129 MB
+L2, so every step's data is cold (inputs larger than L2).  The latency of one
+step alone is also reported: one graph replay between two events after an L2
+flush (a 512 MB write, then a 512 MB read, so the L2 holds only clean,
+unrelated lines).  Per-kernel times
 come from K more steps launched without a graph, with a CUDA event recorded
 on the launching stream before and after every call; all of it is enqueued
 behind the flush, so the calls run back to back as in the graph.  (Event
@@ -33,6 +36,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import math
 import json
 import os
 import statistics
@@ -50,6 +54,8 @@ import workloads as W  # noqa: E402
 
 METRIC = "dispatch/combine µs/call and effective HBM GB/s (1 GB300), % of HBM peak"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6        # GB300 L2
+MAX_SETS = 256
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -343,6 +349,37 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     alone_fns = [(n, fn) for n, fn, _, _ in stages] + [("combine_src", do_combine_src)]
     graphs = {"step": capture(do_step)}
+
+    # ---- the timed region: K steps back to back in one graph, step i on set
+    # i % n_sets of its own inputs and outputs, with enough sets that their
+    # data together is at least four times the L2, so every step's data is
+    # cold (inputs larger than L2 instead of a flush between steps).
+    n_sets = max(1, min(MAX_SETS, math.ceil(4 * L2_BYTES / step_bytes)))
+    sets = [(plan, x_d, idx_d, w_d, y_d)]
+    for _ in range(1, n_sets):
+        p2 = ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, cap, fp8=wl.fp8)
+        st2 = stage_d.clone()
+        sets.append((p2, st2[:nx].view(torch.bfloat16).view(wl.T, wl.H),
+                     st2[nx:nx + ni].view(torch.int32).view(wl.T, wl.k),
+                     st2[nx + ni:].view(torch.float32).view(wl.T, wl.k),
+                     torch.randn((plan.R, wl.H), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)))
+
+    def run_set(q):
+        p2, x2, i2, w2, y2 = sets[q]
+        if fused:
+            p2.layout_dispatch(i2, x2, clear_flags=False)
+        else:
+            p2.layout(i2, clear_flags=False)
+            p2.dispatch(x2)
+        p2.combine(y2, w2)
+
+    with torch.cuda.stream(side):
+        for q in range(n_sets):
+            run_set(q)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graphs["timed"] = capture(lambda: [run_set(q % n_sets) for q in range(args.steps)])
+    graphs["warm"] = capture(lambda: [run_set(q % n_sets) for q in range(args.warmup)])
     stream = torch.cuda.current_stream()
 
     def timed(g, n):
@@ -374,19 +411,30 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         for _ in range(20):
             graphs["step"].replay()
         torch.cuda.synchronize()
-    timed(graphs["step"], args.warmup)
+    flush_l2()
+    graphs["warm"].replay()                      # W warm-up steps
+    flush_l2()
     torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps, back to back, one pair of events
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    step_evs = timed(graphs["step"], args.steps)
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream)
+    graphs["timed"].replay()
+    ev_b.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     wall = time.perf_counter() - t0
+    timed_ms = ev_a.elapsed_time(ev_b)
+
+    # ---- latency of one step alone: K more steps, each one graph replay
+    # between two events after its own L2 flush
+    step_evs = timed(graphs["step"], args.steps)
+    torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in step_evs]
 
     # ---- per-kernel times, same flush discipline, K more steps: the calls of
@@ -452,14 +500,16 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     clocks = sampler.stop()
 
     flags = int(plan.layout_out.err_flags.item())
+    for p2, _, _, _, _ in sets[1:]:
+        flags |= int(p2.layout_out.err_flags.item())
     if flags:
         raise RuntimeError(f"device error flags set during the benchmark: {flags:#x}")
-
-    ms_mean = statistics.fmean(step_ms)
+    ms_mean = timed_ms / args.steps
+    lat_mean = statistics.fmean(step_ms)
     e2e_mean = statistics.fmean(e2e_ms)
     e2e_graph_mean = statistics.fmean(e2e_graph_ms)
-    ms_mean, e2e_mean, e2e_graph_mean, wall = max_over_ranks([ms_mean, e2e_mean, e2e_graph_mean, wall], dist,
-                                                             "cuda")
+    ms_mean, lat_mean, e2e_mean, e2e_graph_mean, wall = max_over_ranks(
+        [ms_mean, lat_mean, e2e_mean, e2e_graph_mean, wall], dist, "cuda")
     if dist is not None:
         dist.destroy_process_group()
     if rank != 0:
@@ -491,10 +541,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
                    "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
                    "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
-                   "step_bytes": step_bytes, "l2": "flushed before every timed step (512 MB write, then 512 MB read: cold, clean L2)",
-                   "timing": "CUDA-graph replay of the step, CUDA events per step",
+                   "step_bytes": step_bytes,
+                   "l2": f"inputs larger than L2: the K timed steps rotate over {n_sets} independent sets of inputs "
+                         f"and outputs ({n_sets} x {step_bytes / 1e6:.1f} MB touched, at least 4x the 129 MB L2), "
+                         "L2 flushed once before the timed region; per-kernel and latency figures flush before "
+                         "every call",
+                   "timing": "the K steps in one CUDA graph between two CUDA events on the launching stream",
                    "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine",
                    "parallelism": f"replicas x{world}"},
+        "latency": {"ms_per_step": round(lat_mean, 5),
+                    "how": "one step per CUDA-graph replay between two CUDA events, L2 flushed before each, "
+                           "mean of K"},
         "kernels": per_kernel,
         "kernels_alone": dict(alone, how="each stage launched alone between two CUDA events on the stream, "
                                           "L2 flushed before every call, median of K calls"),
