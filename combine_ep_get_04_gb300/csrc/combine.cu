@@ -201,6 +201,16 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
                 ok = __all_sync(kFull, mbar_wait(&empty[s], (uint32_t)(((i / NS) - 1) & 1)));
                 if (!ok) break;
             }
+            // The row copies need only the slots: arm the stage's byte count
+            // and start them first; the weights (and fp8 scales) follow, and
+            // the one arrive that completes the phase publishes them.
+            if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)__popc(valid) * a.slice_bytes);
+            __syncwarp();
+            if (slot >= 0) {
+                bulk_load(stages + (size_t)s * a.stage_bytes + (size_t)lane * a.slice_bytes,
+                          a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes,
+                          &full[s]);
+            }
             if (lane < a.k) w_s[s * 32 + lane] = w;
             if (lane == 0) mask_s[s] = valid;
             if (FP8 && slot >= 0) {
@@ -212,13 +222,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(valid) * a.slice_bytes);
-            __syncwarp();
-            if (slot >= 0) {
-                bulk_load(stages + (size_t)s * a.stage_bytes + (size_t)lane * a.slice_bytes,
-                          a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes,
-                          &full[s]);
-            }
+            if (lane == 0) mbar_arrive(&full[s]);
         }
         if (!ok) {
             // Copies already issued target this CTA's shared memory: let them
