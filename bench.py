@@ -373,6 +373,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             p2.dispatch(x2)
         p2.combine(y2, w2)
 
+    side.wait_stream(torch.cuda.current_stream())   # the sets' buffers were filled on this stream
     with torch.cuda.stream(side):
         for q in range(n_sets):
             run_set(q)
