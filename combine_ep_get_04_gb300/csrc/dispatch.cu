@@ -11,8 +11,12 @@
 //   bulk copy global->shared of the next unit (mbarrier completion) while the
 //   k bulk copies shared->global of earlier units drain (bulk groups).
 // A unit is a token row, or a slice of it when there are few tokens, so the
-// grid covers every SM.  Each row of x is read from HBM once and written k
-// times; no thread touches the payload on the bf16 path.
+// grid covers every SM.  When there are more units than one resident wave of
+// CTAs, each CTA takes one unit (bf16) or six (fp8) and the overlap of loads
+// and stores comes from the several CTAs resident on each SM; the ring inside
+// a CTA serves the CTAs that take several units.  Each row of x is read from
+// HBM once and written k times; no thread touches the payload on the bf16
+// path.
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
@@ -24,7 +28,8 @@
 // a persistent grid ends on its slowest SMs; a grid of short CTAs lets the
 // block scheduler give more of them to the SMs that free up first.  Tuned:
 // bf16 one unit per CTA (prefill 88.5 -> 80.3 us, group-limited 202 -> 179
-// us), fp8 six (its ten-warp CTAs cost more to start; skewed 98.8 -> 96.8 us).
+// us), fp8 six (its CTAs of fourteen warps cost more to start; skewed 98.8 ->
+// 96.8 us with eight quantiser warps).
 #ifndef EP_BF16_UNITS_PER_CTA
 #define EP_BF16_UNITS_PER_CTA 1
 #endif
