@@ -2,9 +2,13 @@
 """Benchmark of the MoE dispatch / combine hot path on GB300.
 
 One step = ep_get_layout + ep_dispatch + ep_combine over one batch of
-synthetic tokens (workloads.py).  Default workload: "decode" (T=128, H=7168,
-E=256 as 32 partitions x 8, top-8, fp8 e4m3 dispatch into a [256,128,7168]
-capacity buffer, bf16 combine).
+synthetic tokens (workloads.py).  Default workload: "grouped", the largest
+single-GPU configuration (group-limited routing: T=16384 tokens, H=4096 bf16,
+E=128 experts in 8 groups of 16, each token picks the top-4 groups by max
+logit, then the top-8 experts in them; bf16 dispatch into the packed
+expert-major buffer, weighted bf16 combine; 2.4 GB of algorithmic traffic per
+step).  Small batches (decode: T=128, H=7168, E=256, top-8, fp8 into a
+[256,128,7168] capacity buffer) run ep_layout_dispatch + ep_combine instead.
 
 Metric: effective HBM GB/s of the step = algorithmic bytes (what the method
 must move; see algorithmic_bytes) / device time, plus per-kernel us/call, GB/s
@@ -92,7 +96,7 @@ def hbm_peak() -> tuple[float, str]:
 
 KERNEL_SOURCES = {
     "layout": ("layout.cu",),
-    "dispatch": ("dispatch.cu",),
+    "dispatch": ("dispatch.cu", "ring_schedule.h"),
     "layout_dispatch": ("layout_dispatch.cu",),
     "combine": ("combine.cu",),
 }
@@ -210,9 +214,17 @@ def oracle_sample(wl: W.Workload, step_seconds: float = 1.0):
     oracle_step(probe, inp, y)
     per_token = (time.perf_counter() - t0) / probe.T
     T_s = int(max(1, min(wl.T, step_seconds / max(per_token, 1e-9))))
-    sample = wl.shrink(T_s) if T_s < wl.T else wl
-    inp = W.make(sample)
-    y = W.expert_rows(sample.R, sample.H)
+    for _ in range(2):      # the 16-token probe misjudges the per-token cost: measure and rescale
+        sample = wl.shrink(T_s) if T_s < wl.T else wl
+        inp = W.make(sample)
+        y = W.expert_rows(sample.R, sample.H)
+        t0 = time.perf_counter()
+        oracle_step(sample, inp, y)
+        took = time.perf_counter() - t0
+        T_new = int(max(1, min(wl.T, T_s * step_seconds / max(took, 1e-9))))
+        if abs(T_new - T_s) <= 0.25 * T_s:
+            break
+        T_s = T_new
     n_live = int((inp["topk_idx"] >= 0).sum())
     return sample, inp, y, sum(algorithmic_bytes(sample, n_live).values())
 
@@ -242,6 +254,26 @@ def max_over_ranks(vals: list[float], dist=None, device: str = "cpu") -> list[fl
     if dist is not None and dist.is_initialized():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def n_rotating_sets(step_bytes: int) -> int:
+    """Independent input/output sets the timed steps rotate over: enough that
+    their data together is at least four times the L2."""
+    return max(1, min(MAX_SETS, math.ceil(4 * L2_BYTES / step_bytes)))
+
+
+def workload_config(wl: W.Workload, step_bytes: int, world: int) -> dict:
+    """The `config` object of the bench line; both arms print the same one."""
+    n_sets = n_rotating_sets(step_bytes)
+    return {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
+            "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
+            "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
+            "step_bytes": step_bytes,
+            "l2": f"inputs larger than L2: the GPU arm's K timed steps rotate over {n_sets} independent sets of "
+                  f"inputs and outputs ({n_sets} x {step_bytes / 1e6:.1f} MB touched, at least 4x the 129 MB L2), "
+                  "L2 flushed once before the timed region; its per-kernel and latency figures flush before "
+                  "every call.  The CPU oracle arm runs on the host",
+            "parallelism": f"replicas x{world}"}
 
 
 def replica_throughput(step_bytes: int, world: int, ms: float) -> float:
@@ -354,7 +386,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # i % n_sets of its own inputs and outputs, with enough sets that their
     # data together is at least four times the L2, so every step's data is
     # cold (inputs larger than L2 instead of a flush between steps).
-    n_sets = max(1, min(MAX_SETS, math.ceil(4 * L2_BYTES / step_bytes)))
+    n_sets = n_rotating_sets(step_bytes)
     sets = [(plan, x_d, idx_d, w_d, y_d)]
     for _ in range(1, n_sets):
         p2 = ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, cap, fp8=wl.fp8)
@@ -568,21 +600,16 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_mean, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8-e4m3+bf16" if wl.fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
-                   "top_k": wl.k, "partitions": wl.P, "layout": "capacity" if wl.mode == W.CAPACITY else "packed",
-                   "capacity": wl.capacity or None, "payload": "fp8_e4m3" if wl.fp8 else "bf16",
-                   "step_bytes": step_bytes,
-                   "l2": f"inputs larger than L2: the K timed steps rotate over {n_sets} independent sets of inputs "
-                         f"and outputs ({n_sets} x {step_bytes / 1e6:.1f} MB touched, at least 4x the 129 MB L2), "
-                         "L2 flushed once before the timed region; per-kernel and latency figures flush before "
-                         "every call",
-                   "timing": "the K steps in one CUDA graph between two CUDA events on the launching stream",
-                   "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(wl, step_bytes, world),
+        "method": {"timing": "the K steps in one CUDA graph between two CUDA events on the launching stream",
+                   "calls": "ep_layout_dispatch + ep_combine" if fused else "ep_get_layout + ep_dispatch + ep_combine"},
         "latency": {"ms_per_step": round(lat_mean, 5),
                     "how": "one step per CUDA-graph replay between two CUDA events, L2 flushed before each, "
                            "mean of K"},
-        "kernels": per_kernel,
+        "kernels": dict(per_kernel, resolution="completion of a kernel reaches CUDA events in steps of about "
+                                               "2 us on this GPU, so a per-call figure under ~20 us is bound by "
+                                               "that resolution, not by the kernel; kernels_back_to_back holds "
+                                               "the average launch durations"),
         "kernels_alone": dict(alone, how="each stage launched alone between two CUDA events on the stream, "
                                           "L2 flushed before every call, median of K calls"),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
@@ -614,6 +641,9 @@ def run_reference(args, rank: int, world: int) -> dict | None:
     if rank != 0:
         return None
     wl = W.WORKLOADS[args.workload]
+    full = W.make(wl)
+    step_bytes = sum(algorithmic_bytes(wl, int((full["topk_idx"] >= 0).sum())).values())
+    del full
     step_s = min(1.0, max(0.05, args.cpu_seconds * 5 / max(1, args.steps + args.warmup)))
     sample, inp, y, total_bytes = oracle_sample(wl, step_seconds=step_s)
     times = []
@@ -629,8 +659,7 @@ def run_reference(args, rank: int, world: int) -> dict | None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8-e4m3+bf16" if wl.fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "T": wl.T, "H": wl.H, "E": wl.E,
-                   "top_k": wl.k, "partitions": wl.P, "sample_tokens": sample.T},
+        "config": dict(workload_config(wl, step_bytes, world), sample_tokens=sample.T),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"first {sample.T} of {wl.T} tokens of the {wl.name} workload per step, "
                                    f"single-threaded C oracle", "host_cpus": os.cpu_count()},
@@ -644,7 +673,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=tuple(W.WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=tuple(W.WORKLOADS), default="grouped")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",

@@ -32,7 +32,7 @@ EP_ERR_CUDA = 3
 # Every symbol include/ep.h declares.
 EXPORTED = ("ep_recv_rows", "ep_layout_workspace_bytes", "ep_get_layout", "ep_get_layout_static",
             "ep_dispatch", "ep_layout_dispatch", "ep_combine", "ep_combine_fp8", "ep_combine_src_workspace_bytes",
-            "ep_combine_src", "ep_status_string", "ep_last_error", "ep_abi_version")
+            "ep_combine_src", "ep_status_string", "ep_status_str", "ep_last_error", "ep_abi_version")
 
 
 class Shape(ctypes.Structure):
@@ -92,6 +92,8 @@ def load() -> ctypes.CDLL:
     lib.ep_combine_src.argtypes = [sp, vp, vp, i32, vp, vp, vp, vp, vp, ctypes.c_size_t, vp, vp]
     lib.ep_status_string.restype = ctypes.c_char_p
     lib.ep_status_string.argtypes = [ctypes.c_int]
+    lib.ep_status_str.restype = ctypes.c_char_p
+    lib.ep_status_str.argtypes = [ctypes.c_int]
     lib.ep_last_error.restype = ctypes.c_char_p
     lib.ep_last_error.argtypes = []
     lib.ep_abi_version.restype = ctypes.c_int32

@@ -19,6 +19,7 @@
 // path.
 #include "ep_device.cuh"
 #include "ep_kernels.h"
+#include "ring_schedule.h"
 
 // Units each CTA takes when there are more units than one resident wave of
 // CTAs holds (0: a persistent grid of one wave, every CTA looping over an
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
     };
 
     if (lane == 0) {
-        for (int64_t i = 0; i < LA && i < n_mine; ++i) issue_load(i);
+        for (int64_t i = 0; i < ring_prologue_loads(n_mine, LA); ++i) issue_load(i);
     }
 
     // Lane j holds the slot (and weight) of copy j of the next unit, loaded
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
         const int s = (int)(i % NS);
         // Stage (i+LA)%NS was last read by the stores of unit i+LA-NS; at most
         // NS-LA-1 younger store groups may still be reading their stages.
-        if (i + LA < n_mine) {
+        if (ring_issues_ahead(i, n_mine, LA)) {
             bulk_wait_read<NS - LA - 1>();
             __syncwarp();
             if (lane == 0) issue_load(i + LA);
@@ -168,10 +169,11 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
     }
     bulk_wait_all();
     if (!ok) {
-        // Loads still in flight target this CTA's shared memory: let them land
-        // (each wait bounded) before the CTA exits.
+        // Loads still in flight target this CTA's shared memory: those of
+        // units i .. i+LA (unit i+LA was issued before the wait on unit i gave
+        // up).  Let them land (each wait bounded) before the CTA exits.
         if (lane == 0) {
-            for (int64_t r = i; r < i + LA && r < n_mine; ++r) {
+            for (int64_t r = i; r < ring_issued_end(i, n_mine, LA); ++r) {
                 (void)mbar_wait(&bars[r % NS], (uint32_t)((r / NS) & 1));
             }
             if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);

@@ -93,6 +93,8 @@ const char* ep_status_string(ep_status_t st) {
     return "unknown status";
 }
 
+const char* ep_status_str(ep_status_t st) { return ep_status_string(st); }
+
 const char* ep_last_error(void) { return g_last_error.c_str(); }
 
 int64_t ep_recv_rows(const ep_shape_t* shape) {

@@ -11,14 +11,19 @@
 // Scratch: the per-chunk expert histogram (chunks of 1024 routing entries x E
 // experts, 4 bytes each) lives in the file-scope array below.  Every GPU that
 // loads this library holds it until the process exits.  Its device address is
-// looked up once per device, on the first call made while that device is
-// current.  All calls share the array and it keeps the last call's contents;
+// looked up once per device context, on the first call made while that
+// context is current, and cached under the context's process-unique id: a
+// context created later on the same device (after cudaDeviceReset, say)
+// reloads the module, possibly at another address, and gets a fresh lookup.
+// All calls share the array and it keeps the last call's contents;
 // every entry a call reads is first written by the same call, so nothing has
 // to be cleared.  Calls whose work overlaps on the GPU (different streams, or
 // several host threads on one device) race on the array and must be ordered
 // by the caller.
 #include <cstdio>
 #include <mutex>
+
+#include <cuda.h>
 
 #include "ep.h"
 #include "ep_kernels.h"
@@ -33,31 +38,70 @@ static __device__ __align__(256) int32_t g_layout_scratch[kStaticScratchBytes / 
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;   // 0: nothing cached
+    int32_t* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
 ep_status_t static_fail(ep_status_t st, const char* msg) {
     ep::record_last_error(msg);
     return st;
 }
 
-// Device address of g_layout_scratch on the current device, looked up on the
-// first call for that device.
+// Process-unique id of the calling thread's current context (cuCtxGetId,
+// reached through the runtime's driver entry points, so that nothing links
+// the driver library directly); 0 if there is no current context or the
+// driver cannot tell, in which case nothing is cached.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_layout_scratch in the current device's current
+// context: the cached one if it was looked up in this same context, else a
+// fresh cudaGetSymbolAddress (checked), cached under the context's id.
 ep_status_t scratch_for_current_device(int32_t** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return static_fail(EP_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return static_fail(EP_ERR_UNSUPPORTED, "device index out of range");
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_layout_scratch);
-        if (e != cudaSuccess || ptr == nullptr) {
-            return static_fail(EP_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e)
-                                                             : "cudaGetSymbolAddress returned NULL");
-        }
-        g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+    const unsigned long long id = current_context_id();
+    if (id != 0 && g_scratch[dev].ctx_id == id) {
+        *out = g_scratch[dev].ptr;
+        return EP_OK;
     }
-    *out = g_scratch_ptr[dev];
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_layout_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+        g_scratch[dev] = ScratchEntry{};
+        return static_fail(EP_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e)
+                                                         : "cudaGetSymbolAddress returned NULL");
+    }
+    // the lookup makes the device's primary context current if none was
+    g_scratch[dev] = ScratchEntry{current_context_id(), static_cast<int32_t*>(ptr)};
+    *out = static_cast<int32_t*>(ptr);
     return EP_OK;
 }
 

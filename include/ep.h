@@ -113,6 +113,15 @@ EP_API size_t ep_layout_workspace_bytes(const ep_shape_t *shape);
 /*
  * ep_get_layout -- turn top-k routing into the per-expert layout.
  *
+ * Passages: the per-expert token count and the division of experts into
+ * partitions (expert e on partition e / (E/P)) follow the low-latency
+ * dispatch excerpt quoted in "Redundant atomics in internode_ll" (DeepEP
+ * issue #282, question); the order inside an expert follows "Reasons for not
+ * calling NVSHMEM public APIs?" (DeepEP issue #18, answer on low-latency
+ * mode: the data of one expert keeps its order).  The pages do not give the
+ * layout as a separate call; on one GPU the count exchange they describe
+ * becomes this call.
+ *
  * In:  topk_idx   i32 [T, k]  expert of copy (t, j); -1 = masked slot.
  * Out: counts       i32 [E]    copies routed to each expert (true demand,
  *                              also in capacity mode).
@@ -156,8 +165,10 @@ EP_API ep_status_t ep_get_layout(const ep_shape_t *shape, const int32_t *topk_id
  * ceil(T*k / 1024) * E * 4 bytes > 1 MiB (about 2^20 routing entries at
  * E = 256), return EP_ERR_UNSUPPORTED; smaller shapes that need no workspace
  * use none.  The array's device address is looked up on the first call that
- * needs it on each device, with that device current; make that first call
- * before any stream capture.  All calls share the array and it keeps the
+ * needs it in each device context, with that context current, and reused
+ * while the same context lives (a context created later, e.g. after
+ * cudaDeviceReset, gets its own lookup); make that first call before any
+ * stream capture.  All calls share the array and it keeps the
  * last call's contents (each call writes every entry it reads, so nothing
  * needs clearing); calls whose work overlaps on the GPU race on it and must
  * be ordered by the caller.  Allocates nothing.
@@ -229,6 +240,12 @@ EP_API ep_status_t ep_layout_dispatch(const ep_shape_t *shape, const int32_t *to
 
 /*
  * ep_combine -- weighted top-k reduce of expert outputs back to token order.
+ *
+ * Passage: combine is the reverse of dispatch and is measured beside it in
+ * "Pipeline direct NVLink dispatch with triple-buffered prefetch" (DeepEP PR
+ * #693), Validation table (combine GB/s unchanged by the dispatch pipeline,
+ * balanced and unbalanced); the pages do not spell out its arithmetic, which
+ * is read here as the weighted sum of the token's k expert outputs.
  *
  * In:  y        bf16 [R, H] expert outputs in the receive layout, 16-byte
  *               aligned.
@@ -305,6 +322,9 @@ EP_API ep_status_t ep_combine_src(const ep_shape_t *shape, const void *y,
 
 /* Static description of a status code. */
 EP_API const char *ep_status_string(ep_status_t status);
+
+/* The same function under the shorter name of the original interface plan. */
+EP_API const char *ep_status_str(ep_status_t status);
 
 /* Detail of the last non-EP_OK status returned on the calling thread
  * ("" if none).  The pointer stays valid until the next call on this thread. */

@@ -31,6 +31,7 @@ int main(void)
 
     check(ep_abi_version() == 101, "ABI version");
     check(strcmp(ep_status_string(EP_OK), "ok") == 0, "status text");
+    check(strcmp(ep_status_str(EP_ERR_CUDA), ep_status_string(EP_ERR_CUDA)) == 0, "status text alias");
     check(ep_recv_rows(&decode) == 256 * 128, "capacity rows");
     check(ep_recv_rows(&grouped) == 16384 * 8, "packed rows");
     check(ep_layout_workspace_bytes(&grouped) == (size_t)128 * 128 * 4, "layout workspace");

@@ -45,6 +45,8 @@ def test_abi_version_and_status_strings(lib):
     assert lib.ep_abi_version() == 101
     assert lib.ep_status_string(0) == b"ok"
     assert lib.ep_status_string(1) == b"invalid argument"
+    for st in range(5):
+        assert lib.ep_status_str(st) == lib.ep_status_string(st)
 
 
 def test_rows_and_workspace(lib):

@@ -10,6 +10,9 @@ would show; the layout bar is bit-exact, as in the other layout tests.  This
 file is collected last and also runs on its own in a fresh process.
 """
 import ctypes
+import os
+import shutil
+import subprocess
 
 import numpy as np
 import pytest
@@ -99,3 +102,21 @@ def test_static_layout_rejects_shapes_beyond_its_scratch():
     st = lib.ep_get_layout_static(ctypes.byref(shape), *([None] * 9), None, None)
     assert st == _lib.EP_ERR_UNSUPPORTED
     assert b"scratch" in lib.ep_last_error()
+
+
+def test_static_layout_survives_a_device_reset(tmp_path):
+    """A process that resets the device between two calls gets the array of
+    the new context, not an address cached from the destroyed one (a C++
+    program of its own, so the reset does not touch this process's context)."""
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    lib_path = ep.library_path()
+    exe = tmp_path / "static_after_reset"
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17",
+                    "-I", os.path.join(root, "include"), os.path.join(here, "static_after_reset.cu"),
+                    "-o", str(exe), lib_path, "-Xlinker", "-rpath=" + os.path.dirname(lib_path)],
+                   check=True, capture_output=True, text=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "static layout across a reset ok" in res.stdout
