@@ -304,6 +304,91 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     if (!ok && lane == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
 }
 
+// One unit per CTA, bf16 expert outputs, for batches whose units all fit on
+// the GPU at once.  Each row of the unit has its own "full" mbarrier: lane j
+// of the producer warp issues the bulk copy of row j as soon as its own slot
+// is back (no warp-wide step in between), and the consumers accumulate row j
+// as soon as it has landed, in increasing j, so that the sum overlaps the
+// later rows' arrival.  The consumer warps read the slots (for the valid-row
+// mask) and the weights themselves, so that nothing but the rows passes
+// through the producer.
+constexpr uint32_t kUnitBarBytes = 32u * 8u;                       // full[32]
+constexpr uint32_t kUnitWOffset = kUnitBarBytes;                   // [kConsumerWarps][32] weights
+constexpr uint32_t kUnitStageOffset = round128(kUnitWOffset + 128u * kConsumerWarps);
+
+__global__ void __launch_bounds__(kThreads) combine_unit_kernel(const Args a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    float* w_s = reinterpret_cast<float*>(smem + kUnitWOffset);
+    unsigned char* stage = smem + kUnitStageOffset;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t u = blockIdx.x;
+    const int64_t t = u / a.slices;
+    const int sl = (int)(u - t * a.slices);
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int j = 0; j < a.k; ++j) mbar_init(&full[j], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane < a.k) {
+            const int32_t slot = __ldg(a.slot_of + t * a.k + lane);
+            if (slot >= 0 && slot < a.R) {
+                mbar_arrive_expect_tx(&full[lane], a.slice_bytes);
+                bulk_load(stage + (size_t)lane * a.slice_bytes,
+                          a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes,
+                          &full[lane]);
+                // the copy targets this CTA's shared memory: stay until it
+                // has landed (bounded), whatever the consumers do
+                (void)mbar_wait(&full[lane], 0);
+            } else if (slot != -1 && sl == 0 && a.err_flags != nullptr) {
+                atomicOr(a.err_flags, kErrBadSlot);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    bool valid = false;
+    if (lane < a.k) {
+        const int32_t slot = __ldg(a.slot_of + t * a.k + lane);
+        valid = slot >= 0 && slot < a.R;
+        const float w = a.topk_w != nullptr ? __ldg(a.topk_w + t * a.k + lane) : 1.0f;
+        w_s[cw * 32 + lane] = valid ? w : 0.f;
+    }
+    const uint32_t vmask = __ballot_sync(kFull, valid);
+    __syncwarp();
+    const int ctid = tid - 32;
+    const int chunks = (int)(a.slice_bytes / 16);
+    unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
+    for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
+        uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
+        for (int j = 0; j < a.k; ++j) {
+            if (!((vmask >> j) & 1u)) continue;
+            if (!mbar_wait(&full[j], 0)) {
+                if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+                return;
+            }
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + (size_t)j * a.slice_bytes + ch * 16);
+            const float w = w_s[cw * 32 + j];
+            accumulate(acc, f32x2(w, w), v);
+        }
+        uint4 o;
+        o.x = pack_pair_bf16x2(acc[0]);
+        o.y = pack_pair_bf16x2(acc[1]);
+        o.z = pack_pair_bf16x2(acc[2]);
+        o.w = pack_pair_bf16x2(acc[3]);
+        *reinterpret_cast<uint4*>(dst + ch * 16) = o;
+    }
+}
+
 // Number of slices a row of n granules is cut into: the smallest divisor d of
 // n whose slices hold at most max_per granules and give T*d >= want units;
 // slices never drop below min_per granules once one size fits.
@@ -337,10 +422,25 @@ cudaError_t launch_ring(Args& a, int num_sms, cudaStream_t stream) {
     };
     size_t smem = 0;
     int64_t ctas = 0;
-    cudaError_t err = resident(combine_kernel<1, FP8>, 1, smem, ctas);
-    if (err != cudaSuccess) return err;
-    if (a.units <= ctas) {
-        return launch_kernel(true, combine_kernel<1, FP8>, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
+    cudaError_t err;
+    if (!FP8) {
+        smem = kUnitStageOffset + (size_t)a.stage_bytes;
+        err = cudaFuncSetAttribute(combine_unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel, kThreads, smem);
+        if (err != cudaSuccess) return err;
+        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
+        if (a.units <= ctas) {
+            return launch_kernel(true, combine_unit_kernel, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
+        }
+    } else {
+        err = resident(combine_kernel<1, FP8>, 1, smem, ctas);
+        if (err != cudaSuccess) return err;
+        if (a.units <= ctas) {
+            return launch_kernel(true, combine_kernel<1, FP8>, dim3((unsigned)a.units), dim3(kThreads), smem, stream,
+                                 a);
+        }
     }
     err = resident(combine_kernel<kStages, FP8>, kStages, smem, ctas);
     if (err != cudaSuccess) return err;
