@@ -89,22 +89,10 @@ __device__ __forceinline__ float ue8m0_value(uint32_t e) {
     return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
 }
 
-// Two fp32 lanes in one 64-bit register, and the packed two-wide fp32
-// multiply and add of sm_100+ (each lane rounded to nearest on its own, no
-// flush to zero: exactly two __fmul_rn / __fadd_rn, in half the instructions).
+// Two fp32 lanes in one 64-bit register (an accumulator pair).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 __device__ __forceinline__ uint32_t pack_pair_bf16x2(uint64_t pair) {
@@ -113,25 +101,35 @@ __device__ __forceinline__ uint32_t pack_pair_bf16x2(uint64_t pair) {
     return pack_bf16x2(lo, hi);
 }
 
+// acc += w * v on each lane of a pair: an IEEE product rounded to nearest,
+// then an IEEE sum rounded to nearest (__fmul_rn / __fadd_rn, which are never
+// contracted).  The packed two-wide mul.rn.f32x2 + add.rn.f32x2 of sm_100
+// were used first: the compiled code gave exactly the results of
+// fma.rn.f32x2 (one rounding instead of two), and 7 of the tiny workload's
+// 131072 outputs then differed from the definition by one bf16 ulp.
+__device__ __forceinline__ uint64_t madd_pair(uint64_t acc, float w, float vlo, float vhi) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+    return f32x2(__fadd_rn(lo, __fmul_rn(w, vlo)), __fadd_rn(hi, __fmul_rn(w, vhi)));
+}
+
 // Accumulates w * (value(code) * s) for 16 fp8 codes, as 8 lane pairs.
-__device__ __forceinline__ void accumulate_fp8(uint64_t (&acc)[8], uint64_t w2, uint64_t s2, const uint4& v) {
+__device__ __forceinline__ void accumulate_fp8(uint64_t (&acc)[8], float w, float s, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float2 a = e4m3x2_to_float2((uint16_t)(words[q] & 0xffffu));
         const float2 b = e4m3x2_to_float2((uint16_t)(words[q] >> 16));
-        acc[2 * q] = add_f32x2(acc[2 * q], mul_f32x2(w2, mul_f32x2(f32x2(a.x, a.y), s2)));
-        acc[2 * q + 1] = add_f32x2(acc[2 * q + 1], mul_f32x2(w2, mul_f32x2(f32x2(b.x, b.y), s2)));
+        acc[2 * q] = madd_pair(acc[2 * q], w, __fmul_rn(a.x, s), __fmul_rn(a.y, s));
+        acc[2 * q + 1] = madd_pair(acc[2 * q + 1], w, __fmul_rn(b.x, s), __fmul_rn(b.y, s));
     }
 }
 
 // Accumulates w * y for 8 bf16 values, as 4 lane pairs.
-__device__ __forceinline__ void accumulate(uint64_t (&acc)[4], uint64_t w2, const uint4& v) {
+__device__ __forceinline__ void accumulate(uint64_t (&acc)[4], float w, const uint4& v) {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc[q] = add_f32x2(acc[q], mul_f32x2(w2, f32x2(bf16_lo(words[q]), bf16_hi(words[q]))));
-    }
+    for (int q = 0; q < 4; ++q) acc[q] = madd_pair(acc[q], w, bf16_lo(words[q]), bf16_hi(words[q]));
 }
 
 // Warp 0 produces (indices, weights, bulk copies into a ring of NS stages);
@@ -262,7 +260,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
                         const uint4 v =
                             *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
                         const float w = w_s[s * 32 + j], sc = sc_s[(s * 32 + j) * kMaxSliceBlocks + blk];
-                        accumulate_fp8(acc, f32x2(w, w), f32x2(sc, sc), v);
+                        accumulate_fp8(acc, w, sc, v);
                     }
                 }
                 uint4 o0, o1;
@@ -288,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
                 if (valid & (1u << j)) {
                     const uint4 v = *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
                     const float w = w_s[s * 32 + j];
-                    accumulate(acc, f32x2(w, w), v);
+                    accumulate(acc, w, v);
                 }
             }
             uint4 o;
@@ -378,7 +376,7 @@ __global__ void __launch_bounds__(kThreads) combine_unit_kernel(const Args a) {
             }
             const uint4 v = *reinterpret_cast<const uint4*>(stage + (size_t)j * a.slice_bytes + ch * 16);
             const float w = w_s[cw * 32 + j];
-            accumulate(acc, f32x2(w, w), v);
+            accumulate(acc, w, v);
         }
         uint4 o;
         o.x = pack_pair_bf16x2(acc[0]);

@@ -119,6 +119,32 @@ __device__ __forceinline__ uint32_t halves_below(uint32_t w, uint32_t bm2) {
     return ((bm2 | kHalfTop) - (w & kHalfLow)) & ~w & kHalfTop;
 }
 
+// Bounded wait for an mbarrier phase (as mbar_wait) whose polls let the
+// hardware suspend the thread for up to 0.5 us per poll until the phase
+// completes, instead of spinning: the warps that wait here for a chunk of x
+// or for the receive rows would otherwise take issue slots from the warps
+// doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(500u)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_sleep(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
 // Field f (8 bits) of a packed count word.
 __device__ __forceinline__ uint32_t count_field(uint32_t v, int f) { return (v >> (8 * f)) & 0xffu; }
 
@@ -287,36 +313,41 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         ej = __ldg(a.topk_idx + tk0 + lane);
         if (ej < -1 || ej >= a.E) ej = -1;
     }
-    // Per-warp counts of the targets, four 8-bit counts per word: target j < k
-    // counts ids before the token equal to e_j; with the packed layout target
-    // k + j counts the valid ids below e_j (offsets[e_j]).
-    const int n_words = a.N > 2 * kThreadsF ? kWordsPerThread : 1;   // words beyond N hold no id
-    const int n_targets = a.mode == 0 ? 2 * a.k : a.k;
-    for (int g = 0; 4 * g < n_targets; ++g) {
+    // Per-warp counts, four 8-bit counts per word: in group j / 4, the ids
+    // before the token equal to e_j; with the packed layout, in group
+    // g_below + j / 4, the valid ids below e_j (offsets[e_j]).  Fields of
+    // copies beyond k or with e_j < 0 hold counts nobody reads.
+    const bool two_words = a.N > 2 * kThreadsF;                   // words beyond N hold no id
+    const int g_below = (a.k + 3) / 4;
+    for (int j0 = 0; j0 < a.k; j0 += 4) {
         uint32_t acc = 0;
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
-            const int i = 4 * g + f;
-            if (i < n_targets) {
-                const bool below = i >= a.k;
-                const int e = __shfl_sync(kFull, ej, below ? i - a.k : i);
-                uint32_t c = 0;
-                if (e >= 0) {
-                    const uint32_t b = (uint32_t)e * 0x00010001u;
+            const uint32_t b = (uint32_t)max(__shfl_sync(kFull, ej, (j0 + f) & 31), 0) * 0x00010001u;
+            uint32_t c = __popc(halves_equal(word[0], b) & before[0]);
+            if (two_words) c += __popc(halves_equal(word[1], b) & before[1]);
+            acc |= c << (8 * f);
+        }
+        acc = __reduce_add_sync(kFull, acc);
+        if (lane == 0) part_s[(j0 / 4) * kWarpsF + warp] = acc;
+    }
+    if (a.mode == 0) {
+        for (int j0 = 0; j0 < a.k; j0 += 4) {
+            uint32_t acc = 0;
 #pragma unroll
-                    for (int w = 0; w < kWordsPerThread; ++w) {
-                        if (w < n_words) {
-                            const uint32_t m = below ? (e > 0 ? halves_below(word[w], b - 0x00010001u) : 0u)
-                                                     : halves_equal(word[w], b) & before[w];
-                            c += __popc(m);
-                        }
-                    }
+            for (int f = 0; f < 4; ++f) {
+                const int e = __shfl_sync(kFull, ej, (j0 + f) & 31);
+                uint32_t c = 0;
+                if (e > 0) {
+                    const uint32_t bm = (uint32_t)(e - 1) * 0x00010001u;
+                    c = __popc(halves_below(word[0], bm));
+                    if (two_words) c += __popc(halves_below(word[1], bm));
                 }
                 acc |= c << (8 * f);
             }
+            acc = __reduce_add_sync(kFull, acc);
+            if (lane == 0) part_s[(g_below + j0 / 4) * kWarpsF + warp] = acc;
         }
-        acc = __reduce_add_sync(kFull, acc);
-        if (lane == 0) part_s[g * kWarpsF + warp] = acc;
     }
     __syncthreads();
 
@@ -331,10 +362,10 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
 #pragma unroll
             for (int w = 0; w < kWarpsF; ++w) rank += (int32_t)count_field(part_s[(lane / 4) * kWarpsF + w], lane % 4);
             if (a.mode == 0) {
-                const int i = a.k + lane;
+                const int gb = (a.k + 3) / 4 + lane / 4;
                 int32_t lt = 0;
 #pragma unroll
-                for (int w = 0; w < kWarpsF; ++w) lt += (int32_t)count_field(part_s[(i / 4) * kWarpsF + w], i % 4);
+                for (int w = 0; w < kWarpsF; ++w) lt += (int32_t)count_field(part_s[gb * kWarpsF + w], lane % 4);
                 slot = lt + rank;
             } else if (rank < a.cap) {
                 slot = ej * a.cap + rank;
@@ -360,7 +391,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         // bf16: copy j is written by lane 0 of warp j % kWarpsF, straight from
         // the staged slice, up to kWarpsF copies at once
         if (lane == 0 && warp < a.k) {
-            ok = mbar_wait(slots_ready, 0) && mbar_wait(&x_full[0], 0);
+            ok = mbar_wait_sleep(slots_ready, 0) && mbar_wait_sleep(&x_full[0], 0);
             if (ok) {
                 for (int j = warp; j < a.k; j += kWarpsF) {
                     const int32_t slot = slot_s[j];
@@ -386,7 +417,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         const int b_end = min(a.nblk, (c + 1) * kChunkBlocks);
         unsigned char* out_st = in_st + ((a.in_bytes + 127u) & ~127u);
         float* scale_st = reinterpret_cast<float*>(out_st + (uint32_t)a.nblk * 128u);
-        ok = __all_sync(kFull, mbar_wait(&x_full[c], 0));
+        ok = __all_sync(kFull, mbar_wait_sleep(&x_full[c], 0));
         if (ok) {
             const float r448 = recip_448();
             const int b = c * kChunkBlocks + wi * 4 + (lane >> 3), sub = lane & 7;
@@ -427,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         const int b0 = c * kChunkBlocks, nbc = b_end - b0;
         const int64_t s_col0 = (int64_t)sl * a.nblk + b0;
         const bool scale_bulk = !a.ue8m0 && a.nb % 4 == 0 && a.nblk % 4 == 0;
-        if (ok) ok = mbar_wait(slots_ready, 0);
+        if (ok) ok = mbar_wait_sleep(slots_ready, 0);
         if (ok && wi == 0 && lane == 0) {
             for (int j = 0; j < a.k; ++j) {
                 const int32_t slot = slot_s[j];

@@ -1,12 +1,15 @@
 """GPU path vs the CPU oracle, through the C ABI (via the ctypes binding).
 
 Bar: layout, indices, bf16 receive rows and the fp8 payload + scales are
-bit-exact; combine is within |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| (bf16).
-Sizes: every workload at full size (whole outputs where the oracle is fast,
-sampled tokens plus size-independent properties where the inputs are over a
-gigabyte), shrunken workloads, random shapes crossing every tile and chunk
-boundary, and the degenerate cases (T = 0, T = 1, k = 1, k = E, all copies to
-one expert, capacity overflow, bad ids, all-zero blocks).
+bit-exact; combine is within |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| (bf16),
+the documented contract, and is also asserted bit-equal: the kernel adds the
+same fp32 products in the same j order with the same roundings as the oracle,
+so any difference would mean a reordered or contracted operation.
+Sizes: every workload at full size with whole outputs compared (the largest,
+group-limited, moves 2.4 GB per step), shrunken workloads, random shapes
+crossing every tile and chunk boundary, and the degenerate cases (T = 0,
+T = 1, k = 1, k = E, all copies to one expert, capacity overflow, bad ids,
+all-zero blocks).
 """
 import numpy as np
 import pytest
@@ -65,10 +68,15 @@ def assert_layout_equal(g: dict, o: dict):
 
 
 def assert_combine_close(g_bits: np.ndarray, o_bits: np.ndarray):
+    """The tolerance contract, then bit equality (the kernel keeps the oracle's
+    operation order, so a difference is a finding, not rounding noise)."""
     g = oracle.bf16_to_f32(g_bits).astype(np.float64)
     o = oracle.bf16_to_f32(o_bits).astype(np.float64)
-    bad = np.abs(g - o) > ATOL + RTOL * np.abs(o)
-    assert not bad.any(), f"{bad.sum()} elements out of tolerance, max |diff| {np.abs(g - o).max()}"
+    diff = np.abs(g - o)
+    bad = diff > ATOL + RTOL * np.abs(o)
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance, max |diff| {diff.max()}"
+    n_diff = int((g_bits != o_bits).sum())
+    assert n_diff == 0, f"{n_diff} elements differ in their bits (max |diff| {diff.max()}, within tolerance)"
 
 
 # ------------------------------------------------------------------ layout
@@ -188,23 +196,12 @@ def test_dispatch_bf16_shapes(T, H, E, k, cap):
     _dispatch_bf16_case(wl, idx, x, w)
 
 
-def test_dispatch_bf16_full_size_grouped_properties():
-    """Full group-limited size: every copy equals its source row; sampled rows vs the oracle."""
+def test_dispatch_bf16_full_size_grouped():
+    """Full group-limited size (T = 16384, H = 4096, 131072 receive rows):
+    layout and the whole receive buffer against the oracle's, bit for bit."""
     d = W.make("grouped")
     wl = d["wl"]
-    plan = plan_for(wl)
-    x = bf16_dev(d["x"])
-    plan.layout(dev(d["topk_idx"]))
-    recv, _, _ = plan.dispatch(x)
-    slot = plan.layout_out.slot_of
-    assert torch.equal(recv[slot.flatten().long()].view(torch.int16),
-                       x.repeat_interleave(wl.k, dim=0).view(torch.int16))
-    rng = np.random.default_rng(1)
-    sample = np.sort(rng.choice(wl.T, 64, replace=False))
-    sl = slot.cpu().numpy()[sample]
-    o_recv, _ = oracle.dispatch_bf16(d["x"][sample], np.arange(64 * wl.k, dtype=np.int32).reshape(64, wl.k),
-                                     64 * wl.k)
-    np.testing.assert_array_equal(bits(recv[torch.from_numpy(sl.ravel()).long().cuda()]), o_recv)
+    _dispatch_bf16_case(wl, d["topk_idx"], d["x"], d["topk_w"])
 
 
 # --------------------------------------------------------------- fp8 dispatch
@@ -251,22 +248,12 @@ def test_dispatch_fp8_shapes(T, H, E, k):
     _dispatch_fp8_case(wl, idx, x)
 
 
-def test_dispatch_fp8_full_size_skewed_sampled():
+def test_dispatch_fp8_full_size_skewed():
+    """Full skewed size (T = 8192, Zipf routing, 65536 receive rows): every
+    code and scale of the receive buffer against the oracle's, bit for bit."""
     d = W.make("skewed")
     wl = d["wl"]
-    plan = plan_for(wl)
-    plan.layout(dev(d["topk_idx"]))
-    q, s, _ = plan.dispatch(bf16_dev(d["x"]))
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(2)
-    sample = np.sort(rng.choice(wl.T, 96, replace=False))
-    sl = plan.layout_out.slot_of.cpu().numpy()[sample].ravel()
-    n = len(sample)
-    oq, os_, _ = oracle.dispatch_fp8(d["x"][sample], np.arange(n * wl.k, dtype=np.int32).reshape(n, wl.k),
-                                     n * wl.k)
-    rows = torch.from_numpy(sl).long().cuda()
-    np.testing.assert_array_equal(q.view(torch.uint8)[rows].cpu().numpy(), oq)
-    np.testing.assert_array_equal(s[rows].cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    _dispatch_fp8_case(wl, d["topk_idx"], d["x"])
 
 
 # -------------------------------------------------------------------- combine
@@ -280,9 +267,10 @@ def _combine_case(wl: W.Workload, idx, w, y_bits):
     assert_combine_close(bits(out), oracle.combine(y_bits, w, L["slot_of"]))
 
 
-@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", None), ("skewed", 512),
-                                    ("grouped", 1024), ("tiny", 1)])
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", None), ("skewed", None),
+                                    ("grouped", None), ("skewed", 512), ("grouped", 1024), ("tiny", 1)])
 def test_combine_workloads(name, T):
+    """Every workload at full size (and shrunken), whole output against the oracle."""
     wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)
     d = W.make(wl)
     y = W.expert_rows(wl.R, wl.H)
@@ -313,21 +301,6 @@ def test_combine_shapes(T, H, E, k, cap, mask):
                     mode=W.CAPACITY if cap else W.PACKED, capacity=cap or 0)
     y = W.to_bf16_bits((rng.standard_normal((wl.R, H)) * 4).astype(np.float32))
     _combine_case(wl, idx, w, y)
-
-
-def test_combine_full_size_grouped_sampled():
-    d = W.make("grouped")
-    wl = d["wl"]
-    y = W.expert_rows(wl.R, wl.H)
-    plan = plan_for(wl)
-    plan.layout(dev(d["topk_idx"]))
-    out = plan.combine(bf16_dev(y), dev(d["topk_w"]))
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(3)
-    sample = np.sort(rng.choice(wl.T, 256, replace=False))
-    sl = plan.layout_out.slot_of.cpu().numpy()[sample]
-    o = oracle.combine(y, d["topk_w"][sample], sl)
-    assert_combine_close(bits(out)[sample], o)
 
 
 @pytest.mark.parametrize("name", ["tiny", "prefill", "grouped"])
