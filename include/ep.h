@@ -56,7 +56,7 @@ typedef struct CUstream_st *ep_stream_t;
 typedef enum {
     EP_OK = 0,
     EP_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, bad shape       */
-    EP_ERR_UNSUPPORTED = 2,   /* valid but beyond this build's limits, or no
+    EP_ERR_UNSUPPORTED = 2,   /* valid but beyond this library's limits, or no
                                  sm_103 device current                        */
     EP_ERR_CUDA = 3           /* a CUDA runtime call or launch failed         */
 } ep_status_t;
@@ -87,7 +87,7 @@ enum {
                                  skipped                                      */
 };
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define EP_MAX_EXPERTS 1024
 #define EP_MAX_TOPK 32
 
