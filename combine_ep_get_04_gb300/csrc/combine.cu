@@ -329,6 +329,11 @@ __global__ void __launch_bounds__(kThreads) combine_unit_kernel(const Args a) {
     if (tid == 0) {
         for (int j = 0; j < a.k; ++j) mbar_init(&full[j], 1);
         fence_mbar_init();
+        // Before the wait on the previous kernel: pull this token's slots and
+        // weights towards L2 (no effect on what the loads after the wait
+        // return; the L2 is the point of coherence).
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.slot_of + t * a.k) : "memory");
+        if (a.topk_w != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.topk_w + t * a.k) : "memory");
     }
     __syncthreads();
     pdl_wait();

@@ -275,6 +275,17 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         for (int c = 0; c < n_chunks; ++c) mbar_init(&x_full[c], 1);
         mbar_init(slots_ready, 1);
         fence_mbar_init();
+        // Before the wait on the previous kernel: pull this CTA's x slice
+        // and (below) the routing ids towards L2, so that their DRAM (and
+        // page-table) latency overlaps that kernel's tail.  A prefetch has no
+        // effect on what the loads after the wait return: the L2 is the point
+        // of coherence, and writes of the previous kernel land there.
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.x + (int64_t)t * a.H * 2 + (int64_t)sl * a.in_bytes),
+                     "r"(a.in_bytes)
+                     : "memory");
+    }
+    for (int q = tid; q * 32 < a.N; q += kThreadsF) {   // one 128-byte line each
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.topk_idx + q * 32) : "memory");
     }
     pdl_wait();
     if (tid == 0) {   // the slice of x does not depend on the layout: start it first
