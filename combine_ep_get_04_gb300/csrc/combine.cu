@@ -30,6 +30,14 @@
 #ifndef EP_COMBINE_CONSUMER_WARPS
 #define EP_COMBINE_CONSUMER_WARPS 4
 #endif
+// Consumer warps of the one-unit-per-CTA kernel (decode-sized batches).
+// Measured: 8 against 4 took the decode combine from 5.4-6.6 to 5.4 us back
+// to back and the decode step (fused dispatch + combine) from 11.3-11.8 to
+// 9.4 us; 6, 12 and 16 were slower.  The ring keeps 4 (8 there cost 3-6% on
+// the large workloads).
+#ifndef EP_COMBINE_UNIT_CONSUMER_WARPS
+#define EP_COMBINE_UNIT_CONSUMER_WARPS 8
+#endif
 
 namespace ep {
 
@@ -311,10 +319,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
 // mask) and the weights themselves, so that nothing but the rows passes
 // through the producer.
 constexpr uint32_t kUnitBarBytes = 32u * 8u;                       // full[32]
-constexpr uint32_t kUnitWOffset = kUnitBarBytes;                   // [kConsumerWarps][32] weights
-constexpr uint32_t kUnitStageOffset = round128(kUnitWOffset + 128u * kConsumerWarps);
+constexpr int kUnitConsumerWarps = EP_COMBINE_UNIT_CONSUMER_WARPS;
+constexpr int kUnitThreads = 32 * (1 + kUnitConsumerWarps);
+constexpr uint32_t kUnitWOffset = kUnitBarBytes;                   // [kUnitConsumerWarps][32] weights
+constexpr uint32_t kUnitStageOffset = round128(kUnitWOffset + 128u * kUnitConsumerWarps);
 
-__global__ void __launch_bounds__(kThreads) combine_unit_kernel(const Args a) {
+__global__ void __launch_bounds__(kUnitThreads) combine_unit_kernel(const Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     float* w_s = reinterpret_cast<float*>(smem + kUnitWOffset);
@@ -371,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) combine_unit_kernel(const Args a) {
     const int ctid = tid - 32;
     const int chunks = (int)(a.slice_bytes / 16);
     unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
-    for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
+    for (int ch = ctid; ch < chunks; ch += kUnitConsumerWarps * 32) {
         uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
         for (int j = 0; j < a.k; ++j) {
             if (!((vmask >> j) & 1u)) continue;
@@ -431,11 +441,12 @@ cudaError_t launch_ring(Args& a, int num_sms, cudaStream_t stream) {
         err = cudaFuncSetAttribute(combine_unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel, kThreads, smem);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel, kUnitThreads, smem);
         if (err != cudaSuccess) return err;
         ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
         if (a.units <= ctas) {
-            return launch_kernel(true, combine_unit_kernel, dim3((unsigned)a.units), dim3(kThreads), smem, stream, a);
+            return launch_kernel(true, combine_unit_kernel, dim3((unsigned)a.units), dim3(kUnitThreads), smem, stream,
+                                 a);
         }
     } else {
         err = resident(combine_kernel<1, FP8>, 1, smem, ctas);
