@@ -346,22 +346,14 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Fp8Args
         const unsigned char* ib = in_st + (size_t)s * a.in_stride;
         unsigned char* ob = out_st + (size_t)o * a.out_stride;
         float* oscale = reinterpret_cast<float*>(ob + q_bytes);
-        for (int b = qw; b < a.nblk; b += kFp8QuantWarps) {
-            const uint2 v = *reinterpret_cast<const uint2*>(ib + b * 256 + lane * 8);
-            const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
-            float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-            const float sc = block_scale(m, a.ue8m0 != 0, r448);
-            const float rs = __frcp_rn(sc);
-            const uint32_t q01 = pack_e4m3x2(quotient_rn(x0, sc, rs), quotient_rn(x1, sc, rs));
-            const uint32_t q23 = pack_e4m3x2(quotient_rn(x2, sc, rs), quotient_rn(x3, sc, rs));
-            *reinterpret_cast<uint32_t*>(ob + b * 128 + lane * 4) = q01 | (q23 << 16);
-            if (lane == 0) {
+        // four blocks per warp, eight lanes per block
+        for (int b0 = qw * 4; b0 < a.nblk; b0 += 4 * kFp8QuantWarps) {
+            const BlockScale r = quantize_blocks_8lanes(ib, ob, b0, a.nblk, a.ue8m0 != 0, r448);
+            if (r.first) {
                 if (a.ue8m0) {
-                    ob[q_bytes + b] = ue8m0_byte(sc);
+                    ob[q_bytes + r.b] = ue8m0_byte(r.sc);
                 } else {
-                    oscale[b] = sc;
+                    oscale[r.b] = r.sc;
                 }
             }
         }

@@ -198,4 +198,51 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Quantises up to four 128-channel blocks per warp, eight lanes per block:
+// lanes 8g..8g+7 take block b0 + g (if below b_end), 16 consecutive bf16
+// channels each from in_st + block * 256, find the block's amax in three
+// shuffles within the eight lanes, and write their 16 e4m3 codes to
+// code_st + block * 128.  Every lane of the warp must call it (the shuffles).
+// Returns the block's scale in .sc; .first is set on the lane that should
+// store it (lane 8g, live block), .b is the block.
+struct BlockScale {
+    float sc;
+    int b;
+    bool first;
+};
+
+__device__ __forceinline__ BlockScale quantize_blocks_8lanes(const unsigned char* in_st, unsigned char* code_st, int b0,
+                                                            int b_end, bool ue8m0, float r448) {
+    const int lane = threadIdx.x & 31;
+    const int b = b0 + (lane >> 3), sub = lane & 7;
+    const bool live = b < b_end;
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+    if (live) {
+        v0 = *reinterpret_cast<const uint4*>(in_st + b * 256 + sub * 32);
+        v1 = *reinterpret_cast<const uint4*>(in_st + b * 256 + sub * 32 + 16);
+    }
+    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float xv[16];
+    float m = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        xv[2 * q] = bf16_lo(wv[q]);
+        xv[2 * q + 1] = bf16_hi(wv[q]);
+        m = fmaxf(m, fmaxf(fabsf(xv[2 * q]), fabsf(xv[2 * q + 1])));
+    }
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    const float sc = block_scale(m, ue8m0, r448);
+    const float rs = __frcp_rn(sc);
+    uint32_t code[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = pack_e4m3x2(quotient_rn(xv[4 * q], sc, rs), quotient_rn(xv[4 * q + 1], sc, rs));
+        const uint32_t hi = pack_e4m3x2(quotient_rn(xv[4 * q + 2], sc, rs), quotient_rn(xv[4 * q + 3], sc, rs));
+        code[q] = lo | (hi << 16);
+    }
+    if (live) *reinterpret_cast<uint4*>(code_st + b * 128 + sub * 16) = make_uint4(code[0], code[1], code[2], code[3]);
+    return BlockScale{sc, b, live && sub == 0};
+}
+
 }  // namespace ep

@@ -430,38 +430,9 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         float* scale_st = reinterpret_cast<float*>(out_st + (uint32_t)a.nblk * 128u);
         ok = __all_sync(kFull, mbar_wait_sleep(&x_full[c], 0));
         if (ok) {
-            const float r448 = recip_448();
-            const int b = c * kChunkBlocks + wi * 4 + (lane >> 3), sub = lane & 7;
-            const bool live = b < b_end;
-            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-            if (live) {
-                v0 = *reinterpret_cast<const uint4*>(in_st + b * 256 + sub * 32);
-                v1 = *reinterpret_cast<const uint4*>(in_st + b * 256 + sub * 32 + 16);
-            }
-            const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            float xv[16];
-            float m = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                xv[2 * q] = bf16_lo(wv[q]);
-                xv[2 * q + 1] = bf16_hi(wv[q]);
-                m = fmaxf(m, fmaxf(fabsf(xv[2 * q]), fabsf(xv[2 * q + 1])));
-            }
-#pragma unroll
-            for (int d = 4; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-            const float sc = block_scale(m, a.ue8m0 != 0, r448);
-            const float rs = __frcp_rn(sc);
-            uint32_t code[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t lo = pack_e4m3x2(quotient_rn(xv[4 * q], sc, rs), quotient_rn(xv[4 * q + 1], sc, rs));
-                const uint32_t hi = pack_e4m3x2(quotient_rn(xv[4 * q + 2], sc, rs), quotient_rn(xv[4 * q + 3], sc, rs));
-                code[q] = lo | (hi << 16);
-            }
-            if (live) {
-                *reinterpret_cast<uint4*>(out_st + b * 128 + sub * 16) = make_uint4(code[0], code[1], code[2], code[3]);
-                if (sub == 0) scale_st[b] = sc;
-            }
+            const BlockScale r = quantize_blocks_8lanes(in_st, out_st, c * kChunkBlocks + wi * 4, b_end, a.ue8m0 != 0,
+                                                        recip_448());
+            if (r.first) scale_st[r.b] = r.sc;
             fence_proxy_async_smem();
         }
         // the chunk's warps have all written (or all given up)
