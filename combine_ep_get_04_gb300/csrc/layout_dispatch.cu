@@ -548,22 +548,17 @@ cudaError_t launch_layout_dispatch(const FusedLaunch& f, int num_sms, cudaStream
         n_aux = (int)((fill + EP_FUSED_FILL_BYTES_PER_AUX - 1) / EP_FUSED_FILL_BYTES_PER_AUX);
         if (n_aux > EP_FUSED_MAX_AUX) n_aux = EP_FUSED_MAX_AUX;
     }
-    // With fewer CTAs than SMs, more aux CTAs take the remaining SMs: the
-    // grid then holds one CTA on every SM, and the CTAs of the next kernel,
-    // launched early (programmatic serialization), spread one per SM too
-    // instead of piling onto the SMs this grid left empty.
-    if (a.units + n_aux < num_sms) n_aux = num_sms - a.units;
     if (f.mode != 0 && n_aux > f.E) n_aux = f.E;   // every capacity-mode aux CTA marks at least one expert
     if (n_aux < 1) n_aux = 1;
     // shared memory: head, the x slice, and (fp8) the output stage: codes + f32 scales
     size_t smem = fused_head_bytes(f.E) + ((a.in_bytes + 127u) & ~127u);
     if (f.fp8) smem += ((uint32_t)a.nblk * 132u + 127u) & ~127u;
     // More than half of an SM's shared memory, so that at most one CTA of
-    // this kernel is resident per SM.  The grid holds one CTA per SM; the
-    // next launch of this kernel (started early, programmatic serialization)
-    // then takes each SM as its CTA there finishes, instead of stacking
-    // several early CTAs on a few SMs (measured: 4.4 us back to back on the
-    // decode workload, against 7.5-8 us without the reservation).
+    // this kernel is resident per SM: the next launch of this kernel (started
+    // early, programmatic serialization) then takes each SM as its CTA there
+    // finishes, instead of stacking several early CTAs on the SMs this grid
+    // left idle (measured on the decode workload: 3.8-4.4 us back to back
+    // with the reservation, 7.5-8 us without).
     int dev = 0, smem_sm = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
