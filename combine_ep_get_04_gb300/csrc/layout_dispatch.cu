@@ -119,32 +119,6 @@ __device__ __forceinline__ uint32_t halves_below(uint32_t w, uint32_t bm2) {
     return ((bm2 | kHalfTop) - (w & kHalfLow)) & ~w & kHalfTop;
 }
 
-// Bounded wait for an mbarrier phase (as mbar_wait) whose polls let the
-// hardware suspend the thread for up to 0.5 us per poll until the phase
-// completes, instead of spinning: the warps that wait here for a chunk of x
-// or for the receive rows would otherwise take issue slots from the warps
-// doing the work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(500u)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait_sleep(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
-}
-
 // Field f (8 bits) of a packed count word.
 __device__ __forceinline__ uint32_t count_field(uint32_t v, int f) { return (v >> (8 * f)) & 0xffu; }
 
@@ -402,7 +376,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         // bf16: copy j is written by lane 0 of warp j % kWarpsF, straight from
         // the staged slice, up to kWarpsF copies at once
         if (lane == 0 && warp < a.k) {
-            ok = mbar_wait_sleep(slots_ready, 0) && mbar_wait_sleep(&x_full[0], 0);
+            ok = mbar_wait(slots_ready, 0) && mbar_wait(&x_full[0], 0);
             if (ok) {
                 for (int j = warp; j < a.k; j += kWarpsF) {
                     const int32_t slot = slot_s[j];
@@ -428,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         const int b_end = min(a.nblk, (c + 1) * kChunkBlocks);
         unsigned char* out_st = in_st + ((a.in_bytes + 127u) & ~127u);
         float* scale_st = reinterpret_cast<float*>(out_st + (uint32_t)a.nblk * 128u);
-        ok = __all_sync(kFull, mbar_wait_sleep(&x_full[c], 0));
+        ok = __all_sync(kFull, mbar_wait(&x_full[c], 0));
         if (ok) {
             const BlockScale r = quantize_blocks_8lanes(in_st, out_st, c * kChunkBlocks + wi * 4, b_end, a.ue8m0 != 0,
                                                         recip_448());
@@ -440,7 +414,7 @@ __global__ void __launch_bounds__(kThreadsF) layout_dispatch_kernel(const FusedA
         const int b0 = c * kChunkBlocks, nbc = b_end - b0;
         const int64_t s_col0 = (int64_t)sl * a.nblk + b0;
         const bool scale_bulk = !a.ue8m0 && a.nb % 4 == 0 && a.nblk % 4 == 0;
-        if (ok) ok = mbar_wait_sleep(slots_ready, 0);
+        if (ok) ok = mbar_wait(slots_ready, 0);
         if (ok && wi == 0 && lane == 0) {
             for (int j = 0; j < a.k; ++j) {
                 const int32_t slot = slot_s[j];

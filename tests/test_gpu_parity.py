@@ -362,6 +362,9 @@ FUSED_CASES = [
     (17, 2048, 32, 8, 4, 3, False, 0.05, True),
     (60, 1024, 64, 32, 4, None, True, 0.05, False),      # fp8, k = 32: four passes of eight copies
     (96, 2048, 128, 16, 8, 8, True, 0.0, True),          # fp8 into a capacity buffer that overflows
+    (2048, 256, 64, 1, 4, None, False, 0.05, False),     # T = 2048 (the fused limit), k = 1: more units than SMs
+    (2048, 768, 32, 1, 2, 64, True, 0.0, False),         # the same with fp8 (6 blocks, one chunk) and capacity drops
+    (80, 7680, 1024, 3, 8, None, True, 0.0, True),       # fp8, 60 blocks per row: five full chunks of 12
 ]
 
 
