@@ -120,6 +120,37 @@ def test_host_checks_before_device(lib):
     assert lib.ep_combine_src(ctypes.byref(z), None, None, 0, *([None] * 5), 0, None, None) == 0
 
 
+def test_layout_dispatch_host_checks(lib):
+    """ep_layout_dispatch checks its arguments on the host, before any launch,
+    on the fused path (small batches) and on the two-call path."""
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: rejected on the host
+    odd = ctypes.c_void_p(0x10002)
+
+    def call(shape, x=fake, payload=0, recv=fake, scales=None, recv_w=None, topk_w=None, idx=fake, counts=fake):
+        return lib.ep_layout_dispatch(ctypes.byref(shape), idx, x, topk_w, payload, counts, fake, fake, fake,
+                                      fake, fake, fake, recv, scales, recv_w, None, 0, None, None)
+
+    small = _lib.Shape(4, 128, 16, 4, 1, 0, 0)
+    assert call(small, payload=7) == _lib.EP_ERR_INVALID_ARG               # unknown payload
+    assert call(small, x=None) == _lib.EP_ERR_INVALID_ARG                  # NULL x
+    assert call(small, idx=None) == _lib.EP_ERR_INVALID_ARG                # NULL topk_idx
+    assert call(small, counts=None) == _lib.EP_ERR_INVALID_ARG             # NULL layout output
+    assert call(small, x=odd) == _lib.EP_ERR_INVALID_ARG                   # misaligned x
+    assert call(small, recv=odd) == _lib.EP_ERR_INVALID_ARG                # misaligned recv
+    assert call(small, payload=1) == _lib.EP_ERR_INVALID_ARG               # fp8 without scales
+    assert call(small, payload=1, scales=odd) == _lib.EP_ERR_INVALID_ARG   # misaligned f32 scales
+    assert call(small, recv_w=fake) == _lib.EP_ERR_INVALID_ARG             # recv_w without topk_w
+    h64 = _lib.Shape(4, 64, 16, 4, 1, 0, 0)
+    assert call(h64, payload=1, scales=fake) == _lib.EP_ERR_INVALID_ARG    # fp8 needs H % 128 == 0
+    bad = _lib.Shape(4, 128, 16, 17, 1, 0, 0)
+    assert call(bad) == _lib.EP_ERR_INVALID_ARG                            # k > E
+    assert lib.ep_last_error()
+    # beyond the fused limit: the two-call path rejects a short workspace
+    big = _lib.Shape(8192, 128, 16, 8, 1, 0, 0)
+    assert call(big) == _lib.EP_ERR_INVALID_ARG
+    assert b"workspace" in lib.ep_last_error()
+
+
 def test_product_path_does_not_use_the_oracle():
     """The package never imports the oracle or any CPU fallback."""
     pkg = os.path.join(ROOT, "combine_ep_get_04_gb300")
