@@ -380,6 +380,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         plan.combine_src(y_d, row_w_d)
 
     alone_fns = [(n, fn) for n, fn, _, _ in stages] + [("combine_src", do_combine_src)]
+    if wl.fp8:
+        # combine over fp8 expert outputs: the dispatched codes and scales
+        # themselves stand for the experts' outputs (ep_combine_fp8)
+        def do_combine_fp8():
+            plan.combine_fp8(plan.recv, plan.recv_scales, w_d)
+
+        alone_fns.append(("combine_fp8", do_combine_fp8))
     graphs = {"step": capture(do_step)}
     if args.profile:
         # Only the step kernels, on one set of inputs (for ncu launch lists and
@@ -440,10 +447,18 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             p2.dispatch(x2)
         elif n == "layout_dispatch":
             p2.layout_dispatch(i2, x2, clear_flags=False)
-        else:
+        elif n == "combine":
             p2.combine(y2, w2)
+        elif n == "combine_src":
+            p2.combine_src(y2, row_w_d)
+        else:   # combine_fp8: the set's dispatched codes and scales stand for the expert outputs
+            p2.combine_fp8(p2.recv, p2.recv_scales, w2)
 
-    for n in names:
+    variants = ("combine_src", "combine_fp8") if wl.fp8 else ("combine_src",)
+    for n in variants:          # one eager call each before capture
+        stage_call(n, 0)
+    torch.cuda.synchronize()
+    for n in names + variants:
         graphs["b2b_" + n] = capture(lambda n=n: [stage_call(n, q % n_sets) for q in range(args.steps)])
     graphs["warm"] = capture(lambda: [run_set(q % n_sets) for q in range(args.warmup)])
     stream = torch.cuda.current_stream()
@@ -506,7 +521,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         for q, n in enumerate(names):
             kernel_ms[n].append(evs[q].elapsed_time(evs[q + 1]))
     b2b_us = {}
-    for n in names:
+    for n in names + variants:
         flush_l2()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -653,17 +668,19 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         r.update(bytes=nbytes[name], gbs=round(gbs, 1), frac_of_hbm=round(gbs / peak, 4))
     # combine through the source maps reads each live row's (token, position,
     # weight) record instead of the token-side slot and weight
-    nbytes_alone = dict(nbytes, combine_src=kbytes["combine"] - 8 * wl.T * wl.k + 12 * n_live)
+    nbytes_alone = dict(nbytes, combine_src=kbytes["combine"] - 8 * wl.T * wl.k + 12 * n_live,
+                        combine_fp8=n_live * wl.H + n_live * (wl.H // 128) * 4 + wl.T * wl.H * 2 + wl.T * wl.k * 8)
     alone = {}
     for name, ms in alone_ms.items():
         a_us = statistics.median(ms) * 1e3
         a_gbs = nbytes_alone[name] / (a_us * 1e-6) / 1e9
         alone[name] = dict(us=round(a_us, 3), bytes=nbytes_alone[name], gbs=round(a_gbs, 1),
                            frac_of_hbm=round(a_gbs / peak, 4))
-    b2b = {}
+    b2b, b2b_var = {}, {}
     for name, us in b2b_us.items():
-        gbs = nbytes[name] / (us * 1e-6) / 1e9
-        b2b[name] = dict(us=round(us, 3), gbs=round(gbs, 1), frac_of_hbm=round(gbs / peak, 4))
+        gbs = nbytes_alone[name] / (us * 1e-6) / 1e9
+        (b2b if name in names else b2b_var)[name] = dict(us=round(us, 3), gbs=round(gbs, 1),
+                                                        frac_of_hbm=round(gbs / peak, 4))
     dominant = max(names, key=lambda n: b2b_us[n])
     ach = nbytes[dominant] / (b2b_us[dominant] * 1e-6) / 1e9
     traffic = ncu_traffic(wl.name, dominant)
@@ -692,6 +709,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                                  "rotating sets in one CUDA graph, total / K between two CUDA events"},
         "kernels_back_to_back": dict(b2b, how="each stage K times back to back over the rotating sets (every "
                                               "launch on cold data), one CUDA graph, total / K between two events"),
+        "variants_back_to_back": dict(b2b_var, how="the same for ep_combine_src (combine through the expert-side "
+                                                   "source maps and per-row weights) and, for fp8 workloads, "
+                                                   "ep_combine_fp8 over the dispatched codes and scales"),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_pipe_mean, 5),
                 "how": "every step: x, topk_idx and topk_w from one pinned host buffer -> device in one copy, "

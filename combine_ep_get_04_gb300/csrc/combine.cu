@@ -30,6 +30,11 @@
 #ifndef EP_COMBINE_CONSUMER_WARPS
 #define EP_COMBINE_CONSUMER_WARPS 4
 #endif
+// Consumer warps of the ring over fp8 expert outputs (more arithmetic per
+// byte: every code is widened and multiplied by its block scale).
+#ifndef EP_COMBINE_FP8_CONSUMER_WARPS
+#define EP_COMBINE_FP8_CONSUMER_WARPS 4
+#endif
 // Consumer warps of the one-unit-per-CTA kernel (decode-sized batches).
 // Measured: 8 against 4 took the decode combine from 5.4-6.6 to 5.4 us back
 // to back and the decode step (fused dispatch + combine) from 11.3-11.8 to
@@ -58,7 +63,11 @@ __host__ __device__ constexpr uint32_t stages_offset(int ns, bool fp8) {
     return fp8 ? scales_offset(ns) + 32u * kMaxSliceBlocks * 4u * ns : scales_offset(ns);
 }
 constexpr int kConsumerWarps = EP_COMBINE_CONSUMER_WARPS;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
+// the ring's consumer warps and threads per CTA, by payload
+__host__ __device__ constexpr int ring_consumer_warps(bool fp8) {
+    return fp8 ? EP_COMBINE_FP8_CONSUMER_WARPS : kConsumerWarps;
+}
+__host__ __device__ constexpr int ring_threads(bool fp8) { return 32 * (1 + ring_consumer_warps(fp8)); }
 constexpr int kStages = EP_COMBINE_STAGES;
 constexpr uint32_t kStageBytesMax = EP_COMBINE_STAGE_BYTES;   // k rows x slice bytes per stage
 
@@ -121,15 +130,34 @@ __device__ __forceinline__ uint64_t madd_pair(uint64_t acc, float w, float vlo, 
     return f32x2(__fadd_rn(lo, __fmul_rn(w, vlo)), __fadd_rn(hi, __fmul_rn(w, vhi)));
 }
 
-// Accumulates w * (value(code) * s) for 16 fp8 codes, as 8 lane pairs.
-__device__ __forceinline__ void accumulate_fp8(uint64_t (&acc)[8], float w, float s, const uint4& v) {
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+// Both lanes of a pair multiplied, rounded to nearest (mul.rn.f32x2).  Used
+// only where the product feeds another multiply or add_pair: packed multiply
+// followed by a packed add was compiled into a fused multiply-add.
+__device__ __forceinline__ uint64_t mul_pair(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// acc + p on each lane, as two separately rounded fp32 adds.
+__device__ __forceinline__ uint64_t add_pair(uint64_t acc, uint64_t p) {
+    float al, ah, pl, ph;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(al), "=f"(ah) : "l"(acc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(pl), "=f"(ph) : "l"(p));
+    return f32x2(__fadd_rn(al, pl), __fadd_rn(ah, ph));
+}
+
+// Accumulates w * (value(code) * s) for 8 fp8 codes, as 4 lane pairs: the
+// two products packed two-wide, the sum per lane.
+__device__ __forceinline__ void accumulate_fp8(uint64_t (&acc)[4], float w, float s, const uint2& v) {
+    const uint32_t words[2] = {v.x, v.y};
+    const uint64_t s2 = f32x2(s, s), w2 = f32x2(w, w);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
         const float2 a = e4m3x2_to_float2((uint16_t)(words[q] & 0xffffu));
         const float2 b = e4m3x2_to_float2((uint16_t)(words[q] >> 16));
-        acc[2 * q] = madd_pair(acc[2 * q], w, __fmul_rn(a.x, s), __fmul_rn(a.y, s));
-        acc[2 * q + 1] = madd_pair(acc[2 * q + 1], w, __fmul_rn(b.x, s), __fmul_rn(b.y, s));
+        acc[2 * q] = add_pair(acc[2 * q], mul_pair(mul_pair(f32x2(a.x, a.y), s2), w2));
+        acc[2 * q + 1] = add_pair(acc[2 * q + 1], mul_pair(mul_pair(f32x2(b.x, b.y), s2), w2));
     }
 }
 
@@ -145,7 +173,8 @@ __device__ __forceinline__ void accumulate(uint64_t (&acc)[4], float w, const ui
 // back through its "empty" mbarrier, so index loads and copies of later units
 // overlap the arithmetic of earlier ones.
 template <int NS, bool FP8>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
+__global__ void __launch_bounds__(ring_threads(FP8)) combine_kernel(const Args a) {
+    constexpr int kCW = ring_consumer_warps(FP8);
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                     // [NS] data landed
     uint64_t* empty = full + NS;                                            // [NS] stage free again
@@ -165,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kCW);
         }
         fence_mbar_init();
     }
@@ -175,7 +204,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     bool ok = true;
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        // The slot and weight of unit i+1 are loaded while unit i is issued.
+        // The slot and weight of unit i+1 are loaded while unit i is issued;
+        // with fp8 expert outputs the slots run two units ahead and the block
+        // scales of unit i+1 are loaded (from its slot, back by then) while
+        // unit i is issued, so no load latency sits between two units.
         auto load_index = [&](int64_t i, int32_t& slot, float& w) {
             const int64_t t = (first + i * gridDim.x) / a.slices;
             slot = -1;
@@ -185,9 +217,26 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
                 w = a.topk_w != nullptr ? __ldg(a.topk_w + t * a.k + lane) : 1.0f;
             }
         };
-        int32_t next_slot;
-        float next_w;
+        auto load_scales = [&](int64_t i, int32_t slot, float (&sc)[kMaxSliceBlocks]) {
+            if (!a.ue8m0 || slot < 0 || slot >= a.R) return;   // f32 scales go by cp.async below
+            const int sl = (int)((first + i * gridDim.x) % a.slices);
+            const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.slice_blocks;
+#pragma unroll
+            for (int b = 0; b < kMaxSliceBlocks; ++b) {
+                if (b < a.slice_blocks) {
+                    sc[b] = a.ue8m0 ? ue8m0_value(__ldg(static_cast<const uint8_t*>(a.ys) + s0 + b))
+                                    : __ldg(static_cast<const float*>(a.ys) + s0 + b);
+                }
+            }
+        };
+        int32_t next_slot, next2_slot = -1;
+        float next_w, next2_w = 0.f;
+        float sc_cur[kMaxSliceBlocks], sc_next[kMaxSliceBlocks];
         load_index(0, next_slot, next_w);
+        if (FP8) {
+            if (1 < n_mine) load_index(1, next2_slot, next2_w);
+            load_scales(0, next_slot, sc_next);
+        }
         int64_t i = 0;
         for (; i < n_mine; ++i) {
             const int64_t u = first + i * gridDim.x;
@@ -196,7 +245,16 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
             const int s = (int)(i % NS);
             int32_t slot = next_slot;
             float w = next_w;
-            if (i + 1 < n_mine) load_index(i + 1, next_slot, next_w);
+            if (FP8) {
+#pragma unroll
+                for (int b = 0; b < kMaxSliceBlocks; ++b) sc_cur[b] = sc_next[b];
+                next_slot = next2_slot;
+                next_w = next2_w;
+                if (i + 2 < n_mine) load_index(i + 2, next2_slot, next2_w);
+                if (i + 1 < n_mine) load_scales(i + 1, next_slot, sc_next);
+            } else if (i + 1 < n_mine) {
+                load_index(i + 1, next_slot, next_w);
+            }
             if (slot < -1 || slot >= a.R) {
                 if (sl == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrBadSlot);
                 slot = -1;
@@ -220,14 +278,27 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
             if (lane < a.k) w_s[s * 32 + lane] = w;
             if (lane == 0) mask_s[s] = valid;
             if (FP8 && slot >= 0) {
-                const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.slice_blocks;
                 float* dst = sc_s + (s * 32 + lane) * kMaxSliceBlocks;
-                for (int b = 0; b < a.slice_blocks; ++b) {
-                    dst[b] = a.ue8m0 ? ue8m0_value(__ldg(static_cast<const uint8_t*>(a.ys) + s0 + b))
-                                     : __ldg(static_cast<const float*>(a.ys) + s0 + b);
+                if (a.ue8m0) {
+#pragma unroll
+                    for (int b = 0; b < kMaxSliceBlocks; ++b) {
+                        if (b < a.slice_blocks) dst[b] = sc_cur[b];
+                    }
+                } else {
+                    // f32 scales: 4-byte asynchronous copies straight into the
+                    // stage, tracked by the stage's "full" barrier (the
+                    // arrive below raises its pending count until they land),
+                    // so the producer never waits on them
+                    const float* src = static_cast<const float*>(a.ys) + (int64_t)slot * a.nb +
+                                       (int64_t)sl * a.slice_blocks;
+                    for (int b = 0; b < a.slice_blocks; ++b) {
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst + b)), "l"(src + b)
+                                     : "memory");
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
                 }
             }
-            __syncwarp();
+            __syncwarp();   // every lane's arrive-on above precedes lane 0's arrive
             if (lane == 0) mbar_arrive(&full[s]);
         }
         if (!ok) {
@@ -256,39 +327,48 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
         const uint32_t valid = mask_s[s];
         const unsigned char* st = stages + (size_t)s * a.stage_bytes;
         if (FP8) {
-            // 16 channels per step: 16 code bytes in, 32 bf16 bytes out
+            // 8 channels per step (twice the threads of 16): 8 code bytes in,
+            // 16 bf16 bytes out.  A thread takes two steps, kCW*32 apart, in
+            // one pass over the rows: two independent chains of products and
+            // adds to overlap (every code costs a widening and two multiplies).
             unsigned char* dst = a.out + (t * a.row_bytes + (int64_t)sl * a.slice_bytes) * 2;
-            for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
-                const int blk = (ch * 16) / 128;
-                uint64_t acc[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = 0;   // +0.0f in both lanes
+            const int steps = 2 * chunks, stride = kCW * 32;
+            for (int ch = ctid; ch < steps; ch += 2 * stride) {
+                const int ch2 = ch + stride;
+                const bool two = ch2 < steps;
+                const int blk = ch / 16, blk2 = ch2 / 16;
+                uint64_t acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};   // +0.0f in both lanes
                 for (int j = 0; j < a.k; ++j) {
                     if (valid & (1u << j)) {
-                        const uint4 v =
-                            *reinterpret_cast<const uint4*>(st + (size_t)j * a.slice_bytes + ch * 16);
-                        const float w = w_s[s * 32 + j], sc = sc_s[(s * 32 + j) * kMaxSliceBlocks + blk];
-                        accumulate_fp8(acc, w, sc, v);
+                        const unsigned char* row = st + (size_t)j * a.slice_bytes;
+                        const float* scj = sc_s + (s * 32 + j) * kMaxSliceBlocks;
+                        const float w = w_s[s * 32 + j];
+                        const uint2 v = *reinterpret_cast<const uint2*>(row + ch * 8);
+                        const uint2 v2 = two ? *reinterpret_cast<const uint2*>(row + ch2 * 8) : make_uint2(0, 0);
+                        accumulate_fp8(acc, w, scj[blk], v);
+                        if (two) accumulate_fp8(acc2, w, scj[blk2], v2);
                     }
                 }
-                uint4 o0, o1;
-                o0.x = pack_pair_bf16x2(acc[0]);
-                o0.y = pack_pair_bf16x2(acc[1]);
-                o0.z = pack_pair_bf16x2(acc[2]);
-                o0.w = pack_pair_bf16x2(acc[3]);
-                o1.x = pack_pair_bf16x2(acc[4]);
-                o1.y = pack_pair_bf16x2(acc[5]);
-                o1.z = pack_pair_bf16x2(acc[6]);
-                o1.w = pack_pair_bf16x2(acc[7]);
-                *reinterpret_cast<uint4*>(dst + ch * 32) = o0;
-                *reinterpret_cast<uint4*>(dst + ch * 32 + 16) = o1;
+                uint4 o;
+                o.x = pack_pair_bf16x2(acc[0]);
+                o.y = pack_pair_bf16x2(acc[1]);
+                o.z = pack_pair_bf16x2(acc[2]);
+                o.w = pack_pair_bf16x2(acc[3]);
+                *reinterpret_cast<uint4*>(dst + ch * 16) = o;
+                if (two) {
+                    o.x = pack_pair_bf16x2(acc2[0]);
+                    o.y = pack_pair_bf16x2(acc2[1]);
+                    o.z = pack_pair_bf16x2(acc2[2]);
+                    o.w = pack_pair_bf16x2(acc2[3]);
+                    *reinterpret_cast<uint4*>(dst + ch2 * 16) = o;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             continue;
         }
         unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
-        for (int ch = ctid; ch < chunks; ch += kConsumerWarps * 32) {
+        for (int ch = ctid; ch < chunks; ch += kCW * 32) {
             uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
             for (int j = 0; j < a.k; ++j) {
                 if (valid & (1u << j)) {
@@ -310,25 +390,32 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Args a) {
     if (!ok && lane == 0 && a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
 }
 
-// One unit per CTA, bf16 expert outputs, for batches whose units all fit on
-// the GPU at once.  Each row of the unit has its own "full" mbarrier: lane j
-// of the producer warp issues the bulk copy of row j as soon as its own slot
-// is back (no warp-wide step in between), and the consumers accumulate row j
-// as soon as it has landed, in increasing j, so that the sum overlaps the
-// later rows' arrival.  The consumer warps read the slots (for the valid-row
-// mask) and the weights themselves, so that nothing but the rows passes
-// through the producer.
+// One unit per CTA, for batches whose units all fit on the GPU at once.  Each
+// row of the unit has its own "full" mbarrier: lane j of the producer warp
+// issues the bulk copy of row j as soon as its own slot is back (no warp-wide
+// step in between), and the consumers accumulate row j as soon as it has
+// landed, in increasing j, so that the sum overlaps the later rows' arrival.
+// The consumer warps read the slots (for the valid-row mask) and the weights
+// themselves, so that nothing but the rows passes through the producer.  With
+// fp8 expert outputs the producer lane also stages its row's block scales
+// (after starting the copy) and then arrives, which publishes them with the
+// row.
 constexpr uint32_t kUnitBarBytes = 32u * 8u;                       // full[32]
 constexpr int kUnitConsumerWarps = EP_COMBINE_UNIT_CONSUMER_WARPS;
 constexpr int kUnitThreads = 32 * (1 + kUnitConsumerWarps);
 constexpr uint32_t kUnitWOffset = kUnitBarBytes;                   // [kUnitConsumerWarps][32] weights
-constexpr uint32_t kUnitStageOffset = round128(kUnitWOffset + 128u * kUnitConsumerWarps);
+constexpr uint32_t kUnitScaleOffset = round128(kUnitWOffset + 128u * kUnitConsumerWarps);   // fp8: [32][16] f32
+__host__ __device__ constexpr uint32_t unit_stage_offset(bool fp8) {
+    return fp8 ? round128(kUnitScaleOffset + 32u * kMaxSliceBlocks * 4u) : kUnitScaleOffset;
+}
 
+template <bool FP8>
 __global__ void __launch_bounds__(kUnitThreads) combine_unit_kernel(const Args a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     float* w_s = reinterpret_cast<float*>(smem + kUnitWOffset);
-    unsigned char* stage = smem + kUnitStageOffset;
+    float* sc_s = reinterpret_cast<float*>(smem + kUnitScaleOffset);
+    unsigned char* stage = smem + unit_stage_offset(FP8);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -353,10 +440,22 @@ __global__ void __launch_bounds__(kUnitThreads) combine_unit_kernel(const Args a
         if (lane < a.k) {
             const int32_t slot = __ldg(a.slot_of + t * a.k + lane);
             if (slot >= 0 && slot < a.R) {
-                mbar_arrive_expect_tx(&full[lane], a.slice_bytes);
-                bulk_load(stage + (size_t)lane * a.slice_bytes,
-                          a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes, a.slice_bytes,
-                          &full[lane]);
+                unsigned char* dst = stage + (size_t)lane * a.slice_bytes;
+                const unsigned char* src = a.y + (int64_t)slot * a.row_bytes + (int64_t)sl * a.slice_bytes;
+                if (FP8) {
+                    mbar_expect_tx(&full[lane], a.slice_bytes);
+                    bulk_load(dst, src, a.slice_bytes, &full[lane]);
+                    const int64_t s0 = (int64_t)slot * a.nb + (int64_t)sl * a.slice_blocks;
+                    float* sd = sc_s + lane * kMaxSliceBlocks;
+                    for (int b = 0; b < a.slice_blocks; ++b) {
+                        sd[b] = a.ue8m0 ? ue8m0_value(__ldg(static_cast<const uint8_t*>(a.ys) + s0 + b))
+                                        : __ldg(static_cast<const float*>(a.ys) + s0 + b);
+                    }
+                    mbar_arrive(&full[lane]);   // publishes the scales; the phase ends once the row has landed too
+                } else {
+                    mbar_arrive_expect_tx(&full[lane], a.slice_bytes);
+                    bulk_load(dst, src, a.slice_bytes, &full[lane]);
+                }
                 // the copy targets this CTA's shared memory: stay until it
                 // has landed (bounded), whatever the consumers do
                 (void)mbar_wait(&full[lane], 0);
@@ -380,25 +479,48 @@ __global__ void __launch_bounds__(kUnitThreads) combine_unit_kernel(const Args a
     __syncwarp();
     const int ctid = tid - 32;
     const int chunks = (int)(a.slice_bytes / 16);
-    unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes;
-    for (int ch = ctid; ch < chunks; ch += kUnitConsumerWarps * 32) {
-        uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
-        for (int j = 0; j < a.k; ++j) {
-            if (!((vmask >> j) & 1u)) continue;
-            if (!mbar_wait(&full[j], 0)) {
-                if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
-                return;
+    // fp8: steps of 8 codes (8 code bytes in, 16 bf16 bytes out), twice as
+    // many as the 16-byte steps of bf16
+    const int steps = FP8 ? 2 * chunks : chunks;
+    for (int ch = ctid; ch < steps; ch += kUnitConsumerWarps * 32) {
+        if (FP8) {
+            const int blk = ch / 16;
+            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
+            for (int j = 0; j < a.k; ++j) {
+                if (!((vmask >> j) & 1u)) continue;
+                if (!mbar_wait(&full[j], 0)) {
+                    if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+                    return;
+                }
+                const uint2 v = *reinterpret_cast<const uint2*>(stage + (size_t)j * a.slice_bytes + ch * 8);
+                accumulate_fp8(acc, w_s[cw * 32 + j], sc_s[j * kMaxSliceBlocks + blk], v);
             }
-            const uint4 v = *reinterpret_cast<const uint4*>(stage + (size_t)j * a.slice_bytes + ch * 16);
-            const float w = w_s[cw * 32 + j];
-            accumulate(acc, w, v);
+            unsigned char* dst = a.out + (t * a.row_bytes + (int64_t)sl * a.slice_bytes) * 2 + ch * 16;
+            uint4 o;
+            o.x = pack_pair_bf16x2(acc[0]);
+            o.y = pack_pair_bf16x2(acc[1]);
+            o.z = pack_pair_bf16x2(acc[2]);
+            o.w = pack_pair_bf16x2(acc[3]);
+            *reinterpret_cast<uint4*>(dst) = o;
+        } else {
+            uint64_t acc[4] = {0, 0, 0, 0};   // +0.0f in both lanes
+            for (int j = 0; j < a.k; ++j) {
+                if (!((vmask >> j) & 1u)) continue;
+                if (!mbar_wait(&full[j], 0)) {
+                    if (a.err_flags != nullptr) atomicOr(a.err_flags, kErrTimeout);
+                    return;
+                }
+                const uint4 v = *reinterpret_cast<const uint4*>(stage + (size_t)j * a.slice_bytes + ch * 16);
+                accumulate(acc, w_s[cw * 32 + j], v);
+            }
+            unsigned char* dst = a.out + t * a.row_bytes + (int64_t)sl * a.slice_bytes + ch * 16;
+            uint4 o;
+            o.x = pack_pair_bf16x2(acc[0]);
+            o.y = pack_pair_bf16x2(acc[1]);
+            o.z = pack_pair_bf16x2(acc[2]);
+            o.w = pack_pair_bf16x2(acc[3]);
+            *reinterpret_cast<uint4*>(dst) = o;
         }
-        uint4 o;
-        o.x = pack_pair_bf16x2(acc[0]);
-        o.y = pack_pair_bf16x2(acc[1]);
-        o.z = pack_pair_bf16x2(acc[2]);
-        o.w = pack_pair_bf16x2(acc[3]);
-        *reinterpret_cast<uint4*>(dst + ch * 16) = o;
     }
 }
 
@@ -421,45 +543,36 @@ int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t 
 
 template <bool FP8>
 cudaError_t launch_ring(Args& a, int num_sms, cudaStream_t stream) {
-    // If one single-stage CTA per unit fits on the GPU at once (small
-    // batches), launch exactly that: every unit starts immediately.  Otherwise
-    // a persistent grid of kStages-deep rings.
+    // If one CTA per unit fits on the GPU at once (small batches), launch
+    // exactly that (combine_unit_kernel): every unit starts immediately.
+    // Otherwise a persistent grid of kStages-deep rings.
     auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
         smem = stages_offset(ns, FP8) + (size_t)ns * a.stage_bytes;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ring_threads(FP8), smem);
         ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
         return e;
     };
-    size_t smem = 0;
+    size_t smem = unit_stage_offset(FP8) + (size_t)a.stage_bytes;
     int64_t ctas = 0;
-    cudaError_t err;
-    if (!FP8) {
-        smem = kUnitStageOffset + (size_t)a.stage_bytes;
-        err = cudaFuncSetAttribute(combine_unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel, kUnitThreads, smem);
-        if (err != cudaSuccess) return err;
-        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
-        if (a.units <= ctas) {
-            return launch_kernel(true, combine_unit_kernel, dim3((unsigned)a.units), dim3(kUnitThreads), smem, stream,
-                                 a);
-        }
-    } else {
-        err = resident(combine_kernel<1, FP8>, 1, smem, ctas);
-        if (err != cudaSuccess) return err;
-        if (a.units <= ctas) {
-            return launch_kernel(true, combine_kernel<1, FP8>, dim3((unsigned)a.units), dim3(kThreads), smem, stream,
-                                 a);
-        }
+    cudaError_t err = cudaFuncSetAttribute(combine_unit_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel<FP8>, kUnitThreads, smem);
+    if (err != cudaSuccess) return err;
+    ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
+    if (a.units <= ctas) {
+        return launch_kernel(true, combine_unit_kernel<FP8>, dim3((unsigned)a.units), dim3(kUnitThreads), smem, stream,
+                             a);
     }
     err = resident(combine_kernel<kStages, FP8>, kStages, smem, ctas);
     if (err != cudaSuccess) return err;
     const int64_t grid = ctas < a.units ? ctas : a.units;
-    return launch_kernel(false, combine_kernel<kStages, FP8>, dim3((unsigned)grid), dim3(kThreads), smem, stream, a);
+    return launch_kernel(false, combine_kernel<kStages, FP8>, dim3((unsigned)grid), dim3(ring_threads(FP8)), smem,
+                         stream, a);
 }
 
 }  // namespace
