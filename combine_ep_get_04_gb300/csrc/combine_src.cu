@@ -5,12 +5,13 @@
 // "Pipeline direct NVLink dispatch with triple-buffered prefetch" (Summary).
 //
 // The reduce must stay a gather in increasing j per token (the fp32 sum order
-// of ep_combine), so the token-side map is rebuilt first: the workspace is
-// filled with -1, then one thread per row scatters slot[t, j] = r and
-// w[t, j] = row_w[r].  Pairs no row holds stay -1 and add nothing.  The
-// gather itself is the TMA-staged combine kernel, reading y in place.  The
-// inversion moves R * 12 bytes in and T * k * 8 out, small beside the k rows
-// per token the gather reads.
+// of ep_combine), so the token-side map is rebuilt first: one kernel fills it
+// with -1, then one thread per row scatters slot[t, j] = r and w[t, j] =
+// row_w[r].  Pairs no row holds stay -1 and add nothing.  The gather itself is
+// the TMA-staged combine kernel, reading y in place.  The inversion moves
+// R * 12 bytes in and T * k * 8 out, small beside the k rows per token the
+// gather reads.  The three kernels launch with programmatic serialization, so
+// each one's launch overlaps the previous one's tail.
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 
@@ -25,6 +26,7 @@ __global__ void __launch_bounds__(kThreads)
                       const float* __restrict__ row_w, int64_t R, int T, int k, int32_t* __restrict__ slot,
                       float* __restrict__ w, uint32_t* err_flags) {
     pdl_launch_dependents();
+    pdl_wait();   // the map was filled by the previous kernel
     bool bad = false;
     for (int64_t r = (int64_t)blockIdx.x * kThreads + threadIdx.x; r < R; r += (int64_t)gridDim.x * kThreads) {
         const int32_t t = __ldg(src_token + r);
@@ -42,6 +44,13 @@ __global__ void __launch_bounds__(kThreads)
         atomicOr(err_flags, kErrBadSlot);
 }
 
+// slot[i] = -1 for i < n (the pairs no row claims keep it).
+__global__ void __launch_bounds__(kThreads) fill_map_kernel(int32_t* __restrict__ slot, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();   // the previous kernel of the stream may still read the map
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) slot[i] = -1;
+}
+
 }  // namespace
 
 size_t combine_src_map_bytes(int64_t T, int k) { return ((size_t)T * k * 4 + 255) / 256 * 256; }
@@ -50,13 +59,17 @@ cudaError_t launch_combine_src(const CombineSrcParams& p, int num_sms, cudaStrea
     if (p.base.T == 0) return cudaSuccess;
     int32_t* slot = static_cast<int32_t*>(p.workspace);
     float* w = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + combine_src_map_bytes(p.base.T, p.base.k));
-    cudaError_t err = cudaMemsetAsync(slot, 0xff, (size_t)p.base.T * p.base.k * sizeof(int32_t), stream);
+    const int64_t n = (int64_t)p.base.T * p.base.k;
+    const int64_t cap = (int64_t)num_sms * 8;
+    int64_t fill_blocks = (n + kThreads - 1) / kThreads;
+    if (fill_blocks > cap) fill_blocks = cap;
+    cudaError_t err = launch_kernel(true, fill_map_kernel, dim3((unsigned)fill_blocks), dim3(kThreads), 0, stream,
+                                    slot, n);
     if (err != cudaSuccess) return err;
     if (p.base.R > 0) {
         int64_t blocks = (p.base.R + kThreads - 1) / kThreads;
-        const int64_t cap = (int64_t)num_sms * 8;
         if (blocks > cap) blocks = cap;
-        err = launch_kernel(false, invert_src_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p.src_token,
+        err = launch_kernel(true, invert_src_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p.src_token,
                             p.src_k, p.row_w, p.base.R, p.base.T, p.base.k, slot, w, p.base.err_flags);
         if (err != cudaSuccess) return err;
     }
