@@ -433,6 +433,19 @@ __global__ void __launch_bounds__(kUnitThreads) combine_unit_kernel(const Args a
         if (a.topk_w != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.topk_w + t * a.k) : "memory");
     }
     __syncthreads();
+    if (warp == 1 && lane < a.k) {
+        // Still before the wait: pull this unit's row slices towards L2, at
+        // the slots as they read now.  Only an address hint (checked to lie
+        // inside y): if the previous kernel rewrites the slots or y, the loads
+        // after the wait still read the new values, and the prefetch is
+        // wasted.  Relaxed gpu-scope loads keep the hint out of L1.
+        int32_t s;
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(s) : "l"(a.slot_of + t * a.k + lane) : "memory");
+        if (s >= 0 && s < a.R)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         ::"l"(a.y + (int64_t)s * a.row_bytes + (int64_t)sl * a.slice_bytes), "r"(a.slice_bytes)
+                         : "memory");
+    }
     pdl_wait();
 
     if (warp == 0) {
