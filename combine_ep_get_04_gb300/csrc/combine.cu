@@ -24,8 +24,15 @@
 #ifndef EP_COMBINE_STAGE_BYTES
 #define EP_COMBINE_STAGE_BYTES 16384
 #endif
+// Units the slice size aims at, per SM (bf16 and fp8 expert outputs).
+// Measured on the 128-token batches: bf16 rows of 1024 channels combine in
+// 2.0 us back to back as 512 units against 2.4 us as 1024; fp8 rows of 7168
+// in 5.1 us as 896 units against 5.8 us as 512.
 #ifndef EP_COMBINE_UNITS_PER_SM
-#define EP_COMBINE_UNITS_PER_SM 4     // units the slice size aims at, per SM
+#define EP_COMBINE_UNITS_PER_SM 2
+#endif
+#ifndef EP_COMBINE_FP8_UNITS_PER_SM
+#define EP_COMBINE_FP8_UNITS_PER_SM 4
 #endif
 #ifndef EP_COMBINE_CONSUMER_WARPS
 #define EP_COMBINE_CONSUMER_WARPS 4
@@ -70,6 +77,13 @@ __host__ __device__ constexpr int ring_consumer_warps(bool fp8) {
 __host__ __device__ constexpr int ring_threads(bool fp8) { return 32 * (1 + ring_consumer_warps(fp8)); }
 constexpr int kStages = EP_COMBINE_STAGES;
 constexpr uint32_t kStageBytesMax = EP_COMBINE_STAGE_BYTES;   // k rows x slice bytes per stage
+// Stage of the one-unit kernel (all k rows of one unit; no ring).  Measured
+// on the 128-token batch of 7168 channels: 16 KB stages (896 units) combine
+// in 4.3 us back to back, 32 KB (512 units) in 4.8-4.9 us, 64 KB (256) in 5.8.
+#ifndef EP_COMBINE_UNIT_STAGE_BYTES
+#define EP_COMBINE_UNIT_STAGE_BYTES EP_COMBINE_STAGE_BYTES
+#endif
+constexpr uint32_t kUnitStageBytesMax = EP_COMBINE_UNIT_STAGE_BYTES;
 
 struct Args {
     const unsigned char* y;
@@ -554,35 +568,54 @@ int pick_slices(int64_t T, int64_t n, int64_t max_per, int64_t min_per, int64_t 
 }
 
 
+// Cuts each row into slices for stages of at most stage_max bytes (k rows):
+// the fewest slices that give about units_per_sm units per SM.
+void set_slices(Args& a, const CombineParams& p, int num_sms, uint32_t stage_max) {
+    if (p.fp8) {
+        // whole 128-channel blocks (their scales are staged too), at most
+        // kMaxSliceBlocks of them
+        int64_t max_blocks = (int64_t)(stage_max / 128) / p.k;
+        if (max_blocks > kMaxSliceBlocks) max_blocks = kMaxSliceBlocks;
+        a.slices = pick_slices(p.T, a.nb, max_blocks > 0 ? max_blocks : 1, 1,
+                               (int64_t)EP_COMBINE_FP8_UNITS_PER_SM * num_sms);
+        a.slice_blocks = a.nb / a.slices;
+        a.slice_bytes = (uint32_t)a.slice_blocks * 128u;
+    } else {
+        // 16-byte granules, at least 256 bytes a slice once one size fits
+        const int64_t vec16 = a.row_bytes / 16;
+        const int64_t max_per = (int64_t)(stage_max / 16) / p.k;
+        a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, (int64_t)EP_COMBINE_UNITS_PER_SM * num_sms);
+        a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+    }
+    a.stage_bytes = a.slice_bytes * (uint32_t)p.k;
+    a.units = (int64_t)p.T * a.slices;
+}
+
+// If one CTA per unit fits on the GPU at once (small batches), launches
+// exactly that (combine_unit_kernel): every unit starts immediately.
+// Otherwise a persistent grid of kStages-deep rings, over slices cut for the
+// ring's stage size.
 template <bool FP8>
-cudaError_t launch_ring(Args& a, int num_sms, cudaStream_t stream) {
-    // If one CTA per unit fits on the GPU at once (small batches), launch
-    // exactly that (combine_unit_kernel): every unit starts immediately.
-    // Otherwise a persistent grid of kStages-deep rings.
-    auto resident = [&](auto kern, int ns, size_t& smem, int64_t& ctas) -> cudaError_t {
-        smem = stages_offset(ns, FP8) + (size_t)ns * a.stage_bytes;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ring_threads(FP8), smem);
-        ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
-        return e;
-    };
+cudaError_t launch_combine_t(Args& a, const CombineParams& p, int num_sms, cudaStream_t stream) {
+    set_slices(a, p, num_sms, kUnitStageBytesMax);
     size_t smem = unit_stage_offset(FP8) + (size_t)a.stage_bytes;
-    int64_t ctas = 0;
     cudaError_t err = cudaFuncSetAttribute(combine_unit_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_unit_kernel<FP8>, kUnitThreads, smem);
     if (err != cudaSuccess) return err;
-    ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
-    if (a.units <= ctas) {
+    if (per_sm >= 1 && a.units <= (int64_t)num_sms * per_sm) {
         return launch_kernel(true, combine_unit_kernel<FP8>, dim3((unsigned)a.units), dim3(kUnitThreads), smem, stream,
                              a);
     }
-    err = resident(combine_kernel<kStages, FP8>, kStages, smem, ctas);
+    set_slices(a, p, num_sms, kStageBytesMax);
+    smem = stages_offset(kStages, FP8) + (size_t)kStages * a.stage_bytes;
+    err = cudaFuncSetAttribute(combine_kernel<kStages, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<kStages, FP8>, ring_threads(FP8), smem);
+    if (err != cudaSuccess) return err;
+    const int64_t ctas = (int64_t)num_sms * (per_sm < 1 ? 1 : per_sm);
     const int64_t grid = ctas < a.units ? ctas : a.units;
     return launch_kernel(false, combine_kernel<kStages, FP8>, dim3((unsigned)grid), dim3(ring_threads(FP8)), smem,
                          stream, a);
@@ -602,28 +635,13 @@ cudaError_t launch_combine(const CombineParams& p, int num_sms, cudaStream_t str
     a.k = p.k;
     a.nb = p.H / 128;
     if (p.fp8) {
-        // Slices of whole 128-channel blocks (their scales are staged too), at
-        // most kStageBytesMax / k bytes and kMaxSliceBlocks blocks.
         a.ys = p.y_scales;
         a.ue8m0 = p.ue8m0;
         a.row_bytes = p.H;
-        int64_t max_blocks = (int64_t)(kStageBytesMax / 128) / p.k;
-        if (max_blocks > kMaxSliceBlocks) max_blocks = kMaxSliceBlocks;
-        a.slices = pick_slices(p.T, a.nb, max_blocks > 0 ? max_blocks : 1, 1, (int64_t)EP_COMBINE_UNITS_PER_SM * num_sms);
-        a.slice_blocks = a.nb / a.slices;
-        a.slice_bytes = (uint32_t)a.slice_blocks * 128u;
-    } else {
-        // A stage holds k slices; slices of at most kStageBytesMax / k bytes,
-        // at least 256 bytes once one size fits, enough units for ~4 per SM.
-        a.row_bytes = (int64_t)p.H * 2;
-        const int64_t vec16 = a.row_bytes / 16;
-        const int64_t max_per = (int64_t)(kStageBytesMax / 16) / p.k;
-        a.slices = pick_slices(p.T, vec16, max_per > 0 ? max_per : 1, 16, (int64_t)EP_COMBINE_UNITS_PER_SM * num_sms);
-        a.slice_bytes = (uint32_t)(a.row_bytes / a.slices);
+        return launch_combine_t<true>(a, p, num_sms, stream);
     }
-    a.stage_bytes = a.slice_bytes * (uint32_t)p.k;
-    a.units = (int64_t)p.T * a.slices;
-    return p.fp8 ? launch_ring<true>(a, num_sms, stream) : launch_ring<false>(a, num_sms, stream);
+    a.row_bytes = (int64_t)p.H * 2;
+    return launch_combine_t<false>(a, p, num_sms, stream);
 }
 
 }  // namespace ep
