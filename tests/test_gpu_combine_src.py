@@ -104,8 +104,12 @@ def test_combine_src_matches_oracle(T, H, E, k, cap, mask, weighted):
     assert int(plan.layout_out.err_flags.item()) == 0
 
 
-def test_combine_src_ignores_what_the_workspace_held():
-    T, H, E, k, cap = 300, 256, 32, 6, 20
+# Whatever the workspace held must not matter, for the one-unit gather (the
+# first two shapes) and the ring (the last): in-range row numbers of rows that
+# hold other pairs, out-of-range values, maps of earlier calls with other
+# routing, with masked and dropped copies leaving pairs that no row claims.
+@pytest.mark.parametrize("T,H,E,k,cap", [(300, 256, 32, 6, 20), (128, 7168, 256, 8, 128), (2000, 512, 64, 8, 300)])
+def test_combine_src_ignores_what_the_workspace_held(T, H, E, k, cap):
     plan = _plan(T, H, E, k, cap)
     g = torch.Generator(device="cuda").manual_seed(3)
     plan.src_workspace.view(torch.int32)[:] = torch.randint(-2, plan.R + 2, (plan.src_workspace.numel() // 4,),
@@ -128,6 +132,9 @@ def test_combine_src_fp8_matches_oracle(T, H, E, k, cap, ue8m0):
     else:
         s = np.exp(rng.uniform(-8, 8, size=(R, H // 128))).astype(np.float32)
     plan = _plan(T, H, E, k, cap)
+    g = torch.Generator(device="cuda").manual_seed(T)
+    plan.src_workspace.view(torch.int32)[:] = torch.randint(0, R, (plan.src_workspace.numel() // 4,), generator=g,
+                                                           device="cuda", dtype=torch.int32)   # stale rows
     out = plan.combine_src(dev(q).view(torch.float8_e4m3fn), dev(row_w), dev(L["src_token"]), dev(L["src_k"]),
                            y_scales=dev(s))
     got = bits(out)
