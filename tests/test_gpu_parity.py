@@ -303,6 +303,21 @@ def test_combine_shapes(T, H, E, k, cap, mask):
     _combine_case(wl, idx, w, y)
 
 
+# Batch sizes on both sides of the slicing steps (a row cut into 4, 2 or 1
+# slices at 1024 channels, top-4) and of the switch from one resident CTA per
+# unit to the persistent ring (7168 channels, top-8: 7 slices a row, about 152
+# tokens' worth of units resident at once).
+@pytest.mark.parametrize("T,H,E,k", [(151, 1024, 16, 4), (152, 1024, 16, 4), (305, 1024, 16, 4),
+                                     (152, 7168, 256, 8), (153, 7168, 256, 8)])
+def test_combine_around_the_slicing_steps(T, H, E, k):
+    rng = np.random.default_rng(T * 3 + k)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    wl = W.Workload("s", T=T, H=H, E=E, k=k, P=1, routing="uniform", fp8=False, mode=W.PACKED, capacity=0)
+    y = W.to_bf16_bits((rng.standard_normal((wl.R, H)) * 4).astype(np.float32))
+    _combine_case(wl, idx, w, y)
+
+
 @pytest.mark.parametrize("name", ["tiny", "prefill", "grouped"])
 def test_round_trip_identity_experts_full_size(name):
     """combine(dispatch(x)) with softmax weights returns x (sum of weights ~ 1)."""
@@ -503,7 +518,9 @@ def _fp8_expert_outputs(rng, R, H, ue8m0):
 @pytest.mark.parametrize("T,H,E,k,cap,ue8m0,weighted", [
     (128, 7168, 256, 8, 128, False, True), (128, 7168, 256, 8, 128, True, True), (1, 128, 4, 1, None, False, True),
     (9, 384, 8, 3, None, True, False), (200, 1024, 16, 8, None, False, True), (5, 65536, 4, 2, None, True, True),
-    (640, 7168, 256, 8, None, False, True)])
+    (640, 7168, 256, 8, None, False, True),
+    # around the fp8 slicing steps (7 or 4 slices a row) and the switch to the ring
+    (151, 7168, 256, 8, None, False, True), (152, 7168, 256, 8, None, True, True), (300, 7168, 256, 8, None, False, True)])
 def test_combine_fp8_matches_oracle(T, H, E, k, cap, ue8m0, weighted):
     rng = np.random.default_rng(T + H + 31 * ue8m0)
     idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
