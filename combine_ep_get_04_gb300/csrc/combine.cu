@@ -10,10 +10,12 @@
 // valid slot, y[slot_of[t,j]] slice -> shared stage row j, completing on the
 // stage's "full" mbarrier.  A ring of NS stages keeps up to NS units in flight
 // per CTA -- far more bytes than registers could hold -- while consumer warps
-// sum the k staged rows in fp32 (16 bytes per thread per step), store the
-// bf16 result with 16-byte coalesced stores and hand the stage back through
-// its "empty" mbarrier.  No tensor cores: there is no contraction, only k
-// multiply-adds per output element.
+// sum the k staged rows in fp32 (8 output channels per thread per step: 16
+// bytes of bf16 or 8 fp8 codes in), store the bf16 result with 16-byte
+// coalesced stores and hand the stage back through its "empty" mbarrier.
+// Batches whose units all fit on the GPU at once take one unit per CTA
+// instead (combine_unit_kernel).  No tensor cores: there is no contraction,
+// only k multiply-adds per output element.
 #include "ep_device.cuh"
 #include "ep_kernels.h"
 

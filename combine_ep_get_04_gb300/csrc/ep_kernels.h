@@ -11,7 +11,9 @@ namespace ep {
 
 // Launches `kern`; with pdl, under programmatic stream serialization: it may
 // begin while the previous kernel of the stream finishes, and waits
-// (pdl_wait) before it touches global memory.  Used for latency-sized grids
+// (pdl_wait) before it writes global memory or reads what that kernel may
+// write (before the wait it only prefetches into L2, and reads such memory
+// only as an address hint for a prefetch).  Used for latency-sized grids
 // (about one unit of work per CTA), where the launch gap is a large share of
 // the time; large persistent grids launch normally.
 template <typename... KArgs, typename... Args>
