@@ -256,6 +256,14 @@ def max_over_ranks(vals: list[float], dist=None, device: str = "cpu") -> list[fl
     return t.tolist()
 
 
+def percentiles_us(ms: list[float]) -> dict:
+    """10th and 90th percentiles (µs) of per-call times given in ms."""
+    if len(ms) < 2:
+        return dict(us_p10=round(ms[0] * 1e3, 3), us_p90=round(ms[0] * 1e3, 3)) if ms else {}
+    q = statistics.quantiles(ms, n=10, method="inclusive")
+    return dict(us_p10=round(q[0] * 1e3, 3), us_p90=round(q[-1] * 1e3, 3))
+
+
 def n_rotating_sets(step_bytes: int) -> int:
     """Independent input/output sets the timed steps rotate over: enough that
     their data together is at least four times the L2."""
@@ -541,6 +549,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             alone_ms[n].append(a.elapsed_time(b))
     per_kernel = {n: dict(us=round(statistics.median(kernel_ms[n]) * 1e3, 3),
                           us_mean=round(statistics.fmean(kernel_ms[n]) * 1e3, 3),
+                          **percentiles_us(kernel_ms[n]),
                           timed="inside a step launched call by call, events on the stream between the calls")
                   for n in names}
 
@@ -674,7 +683,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     for name, ms in alone_ms.items():
         a_us = statistics.median(ms) * 1e3
         a_gbs = nbytes_alone[name] / (a_us * 1e-6) / 1e9
-        alone[name] = dict(us=round(a_us, 3), bytes=nbytes_alone[name], gbs=round(a_gbs, 1),
+        alone[name] = dict(us=round(a_us, 3), **percentiles_us(ms), bytes=nbytes_alone[name], gbs=round(a_gbs, 1),
                            frac_of_hbm=round(a_gbs / peak, 4))
     b2b, b2b_var = {}, {}
     for name, us in b2b_us.items():

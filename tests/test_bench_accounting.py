@@ -121,3 +121,11 @@ def test_power_cap_is_reported_and_clean_runs_report_nothing():
     r = _sampler(["2070, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active"] * 3).stop()
     assert r["reasons"] == [] and r["sm_mhz"] == 2070.0
     assert bench.ClockSampler(0).stop() is None   # never started: no record
+
+
+def test_per_call_percentiles():
+    ms = [i / 1000 for i in range(1, 101)]        # 1 .. 100 µs
+    p = bench.percentiles_us(ms)
+    assert p["us_p10"] == pytest.approx(10.9) and p["us_p90"] == pytest.approx(90.1)
+    assert bench.percentiles_us([0.005]) == dict(us_p10=5.0, us_p90=5.0)
+    assert bench.percentiles_us([]) == {}
