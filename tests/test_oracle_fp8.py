@@ -1,11 +1,12 @@
 """Pins for the oracle's FP8 e4m3 encoder and its fp8 dispatch.
 
 Pinned against: torch's float8_e4m3fn conversions (an independent library
-implementation of the same format) for every code and for rounding below 464
-(torch does not saturate, so values >= 464 are pinned by the format definition
-instead); hand-worked values in golden/; the quantisation error bound of the
+implementation of the same format) for every code and for rounding below 464,
+exhaustively over every non-negative float32 there (torch does not saturate,
+so values >= 464 are pinned by the format definition instead); hand-worked values in golden/; the quantisation error bound of the
 format; and the amax code property of every block.
 """
+import os
 from fractions import Fraction
 
 import numpy as np
@@ -74,6 +75,34 @@ def test_random_and_one_binade_exhaustive_match_torch():
         bits = np.arange(base, base + (1 << 23), dtype=np.uint32)
         vals = bits.view(np.float32)
         np.testing.assert_array_equal(oracle.e4m3_encode(vals), _torch_e4m3(vals))
+
+
+def _sweep_e4m3(bounds):
+    """Oracle vs torch codes for every float32 bit pattern in [lo, hi), and for
+    the negatives of every 17th of them; (mismatches, first mismatching bits)."""
+    lo, hi = bounds
+    bits = np.arange(lo, hi, dtype=np.uint32)
+    v = bits.view(np.float32)
+    bad = np.flatnonzero(oracle.e4m3_encode(v) != _torch_e4m3(v))
+    neg = -v[::17]
+    bad_neg = np.flatnonzero(oracle.e4m3_encode(neg) != _torch_e4m3(neg))
+    first = int(bits[bad[0]]) if bad.size else (int(bits[::17][bad_neg[0]]) | 0x80000000 if bad_neg.size else -1)
+    return int(bad.size + bad_neg.size), first
+
+
+def test_every_float32_below_464_matches_torch():
+    """Exhaustive: each of the 1.14e9 non-negative float32 values below 464
+    (where torch's conversion rounds without saturating) gets torch's code,
+    i.e. the nearest code with ties to even; negatives on a stride."""
+    import multiprocessing as mp
+    end = int(np.float32(464.0).view(np.uint32))
+    step = 1 << 26
+    ranges = [(lo, min(end, lo + step)) for lo in range(0, end, step)]
+    with mp.get_context("spawn").Pool(min(len(ranges), max(1, len(os.sched_getaffinity(0))))) as pool:
+        results = pool.map(_sweep_e4m3, ranges, chunksize=1)
+    n_bad = sum(r[0] for r in results)
+    firsts = [r[1] for r in results if r[0]]
+    assert n_bad == 0, f"{n_bad} float32 values encode differently, first at bits {firsts[0]:#010x}"
 
 
 def test_saturation_by_definition():
