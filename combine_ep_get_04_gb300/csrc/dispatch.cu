@@ -104,6 +104,21 @@ __global__ void __launch_bounds__(32) dispatch_bf16_kernel(const Bf16Args a) {
 #pragma unroll
         for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
+        // Before the wait on the previous kernel (the layout, which x does
+        // not depend on): pull the slices of x the first loads will read
+        // towards L2, so that their DRAM latency overlaps that kernel.  A
+        // prefetch changes nothing the loads after the wait return (the L2
+        // is the point of coherence).  Measured: layout + dispatch 1.1-1.3 us
+        // shorter back to back on the prefill and group-limited workloads.
+        for (int64_t i = 0; i < ring_prologue_loads(n_mine, LA); ++i) {
+            const int64_t u = first + i * gridDim.x;
+            const int64_t t = u / a.slices;
+            const int sl = (int)(u - t * a.slices);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.x + t * a.row_bytes +
+                                                                           (int64_t)sl * a.slice_bytes),
+                         "r"(a.slice_bytes)
+                         : "memory");
+        }
     }
     __syncwarp();
     pdl_wait();
