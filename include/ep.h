@@ -22,6 +22,13 @@
  *  - All work is enqueued on `stream` (NULL = the legacy default stream).  A
  *    return of EP_OK means the work was enqueued; results are ready once the
  *    stream reaches that point.  Calls are stateless and thread-safe.
+ *  - Most kernels launch with programmatic stream serialization and let the
+ *    next kernel of the stream start early: each waits for the previous
+ *    kernel to complete before it writes memory or reads what that kernel may
+ *    write (before the wait it only prefetches into L2).  A caller's kernel
+ *    that follows and is itself launched programmatically must likewise
+ *    execute griddepcontrol.wait (cudaGridDependencySynchronize) before it
+ *    reads this library's outputs; kernels launched normally need nothing.
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns EP_ERR_INVALID_ARG (unsupported sizes EP_ERR_UNSUPPORTED)
  *    with nothing enqueued.  A failed launch returns EP_ERR_CUDA.  The text of
