@@ -515,6 +515,25 @@ def _fp8_expert_outputs(rng, R, H, ue8m0):
     return q, s
 
 
+def test_combine_fp8_full_size_skewed():
+    """The fp8 combine in the configuration the benchmark times it in: the
+    skewed workload at full size (65536 rows of 7168 e4m3 codes with f32
+    block scales, 8192 tokens, top-8), every token against the oracle."""
+    d = W.make("skewed")
+    wl = d["wl"]
+    rng = np.random.default_rng(23)
+    q = rng.integers(0, 256, size=(wl.R, wl.H), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3A                                   # no NaN codes
+    s = np.exp(rng.uniform(-8, 8, size=(wl.R, wl.H // 128))).astype(np.float32)
+    plan = plan_for(wl)
+    plan.layout(dev(d["topk_idx"]))
+    out = plan.combine_fp8(dev(q).view(torch.float8_e4m3fn), dev(s), dev(d["topk_w"]))
+    torch.cuda.synchronize()
+    assert int(plan.layout_out.err_flags.item()) == 0
+    L = oracle_layout(wl, d["topk_idx"])
+    assert_combine_close(bits(out), oracle.combine_fp8(q, s, d["topk_w"], L["slot_of"]))
+
+
 @pytest.mark.parametrize("T,H,E,k,cap,ue8m0,weighted", [
     (128, 7168, 256, 8, 128, False, True), (128, 7168, 256, 8, 128, True, True), (1, 128, 4, 1, None, False, True),
     (9, 384, 8, 3, None, True, False), (200, 1024, 16, 8, None, False, True), (5, 65536, 4, 2, None, True, True),
