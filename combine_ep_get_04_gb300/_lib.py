@@ -6,9 +6,8 @@ implementation behind these names.
 from __future__ import annotations
 
 import ctypes
+import importlib
 import os
-
-from . import build as _build
 
 PACKED = 0
 CAPACITY = 1
@@ -55,7 +54,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    # imported here, not at package import, so that `python -m
+    # combine_ep_get_04_gb300.build` runs the module fresh
+    return importlib.import_module(__package__ + ".build").LIB_PATH
 
 
 def load() -> ctypes.CDLL:
