@@ -399,15 +399,23 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     if args.profile:
         # Only the step kernels, on one set of inputs (for ncu launch lists and
         # captures, with little device memory): W + K graph replays, each
-        # behind an L2 flush.
+        # behind an L2 flush; with --profile-variant, each followed by one
+        # call of that variant behind its own flush.
+        variant = dict(alone_fns).get(args.profile_variant) if args.profile_variant else None
+        if args.profile_variant and variant is None:
+            raise SystemExit(f"--profile-variant {args.profile_variant}: not run on the {wl.name} workload")
         for _ in range(args.warmup + args.steps):
             flush_l2()
             graphs["step"].replay()
+            if variant is not None:
+                flush_l2()
+                variant()
         torch.cuda.synchronize()
         flags = int(plan.layout_out.err_flags.item())
         if rank == 0:
             print(json.dumps({"profile_run": wl.name, "steps": args.warmup + args.steps,
-                              "launches_per_step": launches_per_step, "err_flags": flags}))
+                              "launches_per_step": launches_per_step, "variant": args.profile_variant,
+                              "err_flags": flags}))
         if dist is not None:
             dist.destroy_process_group()
         return None
@@ -784,6 +792,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=tuple(W.WORKLOADS), default="grouped")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-variant", choices=("combine_src", "combine_fp8"), default=None,
+                    help="with --profile: also run this variant once after every step")
     ap.add_argument("--profile", action="store_true",
                     help="run only W+K flushed step replays (for an ncu launch list); prints no bench line")
     args = ap.parse_args(argv)
