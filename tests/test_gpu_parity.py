@@ -256,6 +256,23 @@ def test_dispatch_fp8_full_size_skewed():
     _dispatch_fp8_case(wl, d["topk_idx"], d["x"])
 
 
+def test_dispatch_fp8_ue8m0_full_size_skewed():
+    """The same full skewed dispatch with power-of-two (UE8M0) scales: every
+    code and exponent byte against the oracle's."""
+    d = W.make("skewed")
+    wl = d["wl"]
+    plan = ep.Plan(wl.T, wl.H, wl.E, wl.k, wl.P, None, fp8=True, scale_fmt="ue8m0")
+    plan.layout(dev(d["topk_idx"]))
+    q, e, _ = plan.dispatch(bf16_dev(d["x"]))
+    torch.cuda.synchronize()
+    assert int(plan.layout_out.err_flags.item()) == 0
+    L = oracle_layout(wl, d["topk_idx"])
+    assert (L["slot_of"] >= 0).all()           # packed, nothing masked: every row holds a copy
+    oq, oe, _ = oracle.dispatch_fp8_ue8m0(d["x"], L["slot_of"], wl.R)
+    np.testing.assert_array_equal(q.view(torch.uint8).cpu().numpy(), oq)
+    np.testing.assert_array_equal(e.cpu().numpy(), oe)
+
+
 # -------------------------------------------------------------------- combine
 
 def _combine_case(wl: W.Workload, idx, w, y_bits):
