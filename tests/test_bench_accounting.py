@@ -32,6 +32,8 @@ EXPECTED = {
     "skewed": dict(dispatch=601_882_624, combine=1_057_488_896),
     # group-limited: T=16384 H=4096 k=8, bf16; layout 2*4*131072 + 8*131072 + 4*(2*128 + 2*8 + 2)
     "grouped": dict(layout=2_098_248, dispatch=1_207_959_552, combine=1_209_008_128),
+    # unbalanced: the skewed shape with milder routing, so the same bytes
+    "unbalanced": dict(dispatch=601_882_624, combine=1_057_488_896),
 }
 
 
@@ -44,13 +46,23 @@ def test_algorithmic_bytes_by_hand(name):
 
 
 @pytest.mark.parametrize("name,n_sets", [("tiny", 196), ("decode", 20), ("prefill", 1), ("skewed", 1),
-                                         ("grouped", 1)])
+                                         ("grouped", 1), ("unbalanced", 1)])
 def test_rotating_sets_cover_four_l2(name, n_sets):
     wl = W.WORKLOADS[name]
     step = sum(bench.algorithmic_bytes(wl, wl.T * wl.k).values())
     n = bench.n_rotating_sets(step)
     assert n == n_sets
     assert n * step >= 4 * bench.L2_BYTES
+
+
+@pytest.mark.parametrize("name,partition,expert", [("skewed", 4.06, 29.7), ("unbalanced", 1.50, 5.59)])
+def test_skewed_routing_imbalance(name, partition, expert):
+    """The two Zipf workloads' imbalance with seed 0: max/mean copies per
+    partition and per expert."""
+    d = W.make(name)
+    st = W.load_stats(d["wl"], d["topk_idx"])
+    assert st["partition_max_over_mean"] == pytest.approx(partition, abs=0.02)
+    assert st["expert_max_over_mean"] == pytest.approx(expert, abs=0.02)
 
 
 def test_config_names_the_workload_and_its_layout():

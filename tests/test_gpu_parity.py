@@ -225,7 +225,8 @@ def _dispatch_fp8_case(wl: W.Workload, idx, x):
     assert int(plan.layout_out.err_flags.item()) & ep.ERRF_TIMEOUT == 0
 
 
-@pytest.mark.parametrize("name,T", [("decode", None), ("skewed", 640), ("decode", 1), ("skewed", 33)])
+@pytest.mark.parametrize("name,T", [("decode", None), ("skewed", 640), ("decode", 1), ("skewed", 33),
+                                    ("unbalanced", None)])
 def test_dispatch_fp8_workloads(name, T):
     wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)
     d = W.make(wl)
@@ -285,7 +286,8 @@ def _combine_case(wl: W.Workload, idx, w, y_bits):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", None), ("skewed", None),
-                                    ("grouped", None), ("skewed", 512), ("grouped", 1024), ("tiny", 1)])
+                                    ("grouped", None), ("unbalanced", None), ("skewed", 512), ("grouped", 1024),
+                                    ("tiny", 1)])
 def test_combine_workloads(name, T):
     """Every workload at full size (and shrunken), whole output against the oracle."""
     wl = W.WORKLOADS[name] if T is None else W.WORKLOADS[name].shrink(T)

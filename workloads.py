@@ -19,6 +19,10 @@ Workloads (shapes of the DeepSeek-V3 MoE layer where named so):
             a seeded permutation, sampled without replacement, fp8, packed
   grouped   T=16384, H=4096, E=128 in 8 groups of 16; top-4 groups by max
             logit, then top-8 experts inside them; bf16, packed
+  unbalanced  as skewed with Zipf(s=0.4): max/mean load 1.50 per partition
+            (5.59 per expert) with seed 0, the rank imbalance of the second
+            Validation table of "Pipeline direct NVLink dispatch with
+            triple-buffered prefetch" (DeepEP PR #693)
 """
 from __future__ import annotations
 
@@ -74,6 +78,10 @@ WORKLOADS: dict[str, Workload] = {
     "grouped": Workload("grouped", T=16384, H=4096, E=128, k=8, P=8, routing="group_limited",
                         fp8=False, groups=8, topk_groups=4,
                         description="T=16384 H=4096 E=128 (8 groups x 16) top-4 groups/top-8, bf16"),
+    "unbalanced": Workload("unbalanced", T=8192, H=7168, E=256, k=8, P=32, routing="zipf", fp8=True,
+                           zipf_s=0.4,
+                           description="T=8192 H=7168 E=256 (32x8) top-8 Zipf(0.4): partition load max/mean 1.5, "
+                                       "fp8 packed"),
 }
 
 # Independent streams, one per tensor.
