@@ -85,6 +85,7 @@ SHAPES = [
     (37, 264, 8, 8, None, 0.2),          # k = E, masked copies, a ragged 528-byte row
     (300, 1024, 32, 6, 20, 0.1),         # capacity overflow: dropped copies
     (2000, 512, 64, 8, None, 0.0),       # more units than resident CTAs (persistent ring)
+    (20, 512, 64, 32, None, 0.1),        # top-32: 32 rows a unit, masked copies
 ]
 
 

@@ -558,7 +558,9 @@ def test_combine_fp8_full_size_skewed():
     (9, 384, 8, 3, None, True, False), (200, 1024, 16, 8, None, False, True), (5, 65536, 4, 2, None, True, True),
     (640, 7168, 256, 8, None, False, True),
     # around the fp8 slicing steps (7 or 4 slices a row) and the switch to the ring
-    (151, 7168, 256, 8, None, False, True), (152, 7168, 256, 8, None, True, True), (300, 7168, 256, 8, None, False, True)])
+    (151, 7168, 256, 8, None, False, True), (152, 7168, 256, 8, None, True, True), (300, 7168, 256, 8, None, False, True),
+    # top-32: 32 staged rows a unit (the one-unit kernel's limit), then the ring
+    (48, 2048, 64, 32, None, False, True), (48, 2048, 64, 32, None, True, False), (700, 1024, 64, 32, None, False, True)])
 def test_combine_fp8_matches_oracle(T, H, E, k, cap, ue8m0, weighted):
     rng = np.random.default_rng(T + H + 31 * ue8m0)
     idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
